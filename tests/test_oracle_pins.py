@@ -1,0 +1,262 @@
+"""Pins for the CPU oracle (CPU only, no GPU).
+
+Each check ties an oracle routine to something other than itself: the pages'
+worked example and trace, a hand-derived tie case, closed forms of the
+evens/odds and heavy-tie workloads, brute force over every tiny sorted input,
+and Python's guaranteed-stable ``sorted`` / numpy's stable argsort as library
+routines.  ``test_oracle_mutants.py`` plants mistakes in a copy of the oracle
+and checks that these pins catch each one.
+
+The check functions take the oracle library handle so the mutant test can run
+them against a mutated build.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ----------------------------------------------------------------- checks --
+
+def check_worked_example(lib):
+    """Co-rank page: trace table, three-thread splits, thread-1 slice."""
+    rows = _read_golden("corank_trace_example.txt")
+    A = [int(x) for x in next(r for r in rows if r[0] == "A")[1:]]
+    B = [int(x) for x in next(r for r in rows if r[0] == "B")[1:]]
+    k = int(next(r for r in rows if r[0] == "k")[1])
+    want_i, want_j = (int(x) for x in next(r for r in rows if r[0] == "result")[1:])
+    i, trace = oracle.corank_pages(k, A, B, trace=True, lib=lib)
+    assert (i, k - i) == (want_i, want_j)
+    want_trace = [r[1:] for r in rows if r[0] == "trace"]
+    assert len(trace) == len(want_trace)
+    for got, want in zip(trace, want_trace):
+        it, i_low, ii, jj, j_low = (int(x) for x in want[:5])
+        a_im1, b_j, b_jm1, a_i = want[5:9]
+        assert (got["i_low"], got["i"], got["j"], got["j_low"]) == (i_low, ii, jj, j_low)
+        # the compared values printed in the table
+        assert int(a_im1) == A[ii - 1] and int(b_j) == B[jj]
+        if b_jm1 != "-":
+            assert int(b_jm1) == B[jj - 1] and int(a_i) == A[ii]
+        assert got["verdict"] == want[9].replace("_", " ")
+        assert got["delta"] == int(want[10])
+    for r in rows:
+        if r[0] == "split":
+            kk, si, sj = (int(x) for x in r[1:])
+            assert oracle.corank_pages(kk, A, B, lib=lib) == si
+            assert oracle.corank_count(kk, A, B, lib=lib) == si
+            assert kk - si == sj
+    C = oracle.merge_i32(A, B, lib=lib)
+    sl = next(r for r in rows if r[0] == "slice")
+    start = int(sl[1])
+    vals = [int(x) for x in sl[2:]]
+    assert list(C[start:start + len(vals)]) == vals
+    assert list(C) == sorted(A + B)
+
+
+def check_tie_case(lib):
+    """Hand-derived tie case on the page's tiny inputs, with sources."""
+    rows = {r[0]: r[1:] for r in _read_golden("tie_case_small.txt")}
+    A = [int(x) for x in rows["A"]]
+    B = [int(x) for x in rows["B"]]
+    C = [int(x) for x in rows["C"]]
+    src = rows["src"]
+    assert list(oracle.merge_i32(A, B, lib=lib)) == C
+    va = [i for i in range(len(A))]
+    vb = [(1 << 31) | i for i in range(len(B))]
+    kc, vc = oracle.merge_pairs_u32(A, va, B, vb, lib=lib)
+    assert list(kc) == C
+    got_src = [("B%d" % (v & 0x7FFFFFFF)) if v >> 31 else ("A%d" % v) for v in vc]
+    assert got_src == src
+    for k in range(len(C)):
+        # co-rank = number of A sources among the first k outputs
+        want_i = sum(1 for s in src[:k] if s[0] == "A")
+        assert oracle.corank_pages(k, A, B, lib=lib) == want_i
+        assert oracle.corank_count(k, A, B, lib=lib) == want_i
+        v, from_a = oracle.merge_at_i32(k, A, B, lib=lib)
+        assert v == C[k] and from_a == (src[k][0] == "A")
+
+
+def _sorted_seqs(max_len, alphabet):
+    for L in range(max_len + 1):
+        yield from itertools.combinations_with_replacement(alphabet, L)
+
+
+def check_brute_force(lib, max_len=5, alphabet=(0, 1, 2)):
+    """Every pair of sorted inputs up to max_len over a 3-letter alphabet:
+    the merge equals Python's stable sort of the tagged concatenation, and
+    both co-rank routines equal the count of A tags among the first k."""
+    seqs = [list(s) for s in _sorted_seqs(max_len, alphabet)]
+    for A in seqs:
+        for B in seqs:
+            tagged = sorted([(a, 0, p) for p, a in enumerate(A)] + [(b, 1, p) for p, b in enumerate(B)],
+                            key=lambda t: t[0])  # sorted() is stable: A's items stay first on ties
+            want = [t[0] for t in tagged]
+            assert list(oracle.merge_i32(A, B, lib=lib)) == want
+            va = list(range(len(A)))
+            vb = [(1 << 31) | p for p in range(len(B))]
+            kc, vc = oracle.merge_pairs_u32(A, va, B, vb, lib=lib)
+            assert list(kc) == want
+            assert list(vc) == [p if s == 0 else (1 << 31) | p for _, s, p in tagged]
+            a_count = 0
+            for k in range(len(A) + len(B) + 1):
+                assert oracle.corank_pages(k, A, B, lib=lib) == a_count, (A, B, k)
+                assert oracle.corank_count(k, A, B, lib=lib) == a_count, (A, B, k)
+                if k < len(want):
+                    v, from_a = oracle.merge_at_i32(k, A, B, lib=lib)
+                    assert v == want[k] and from_a == (tagged[k][1] == 0)
+                    a_count += tagged[k][1] == 0
+
+
+def check_evens_odds_closed_form(lib, scale_log2=0):
+    """Evens/odds workload: with n = len(B) and A = 0,2,4,... longer by t0:
+    C[k] = k for k < 2n, and C[2n + t] = 2n + 2t for the A-only tail;
+    co_rank(k) = ceil(k / 2) for k <= 2n and k - n above."""
+    d = synth.make_host("evens_odds", scale_log2)
+    A, B = d["A"], d["B"]
+    m, n = A.size, B.size
+    C = oracle.merge_i32(A, B, lib=lib)
+    k = np.arange(m + n, dtype=np.int64)
+    want = np.where(k < 2 * n, k, 2 * n + 2 * (k - 2 * n))
+    assert np.array_equal(C.astype(np.int64), want)
+    rng = np.random.default_rng(11)
+    ks = np.concatenate([[0, 1, 2, 2 * n - 1, 2 * n, 2 * n + 1, m + n - 1, m + n],
+                         rng.integers(0, m + n + 1, 64)])
+    for kk in ks:
+        kk = int(kk)
+        want_i = (kk + 1) // 2 if kk <= 2 * n else kk - n
+        assert oracle.corank_pages(kk, A, B, lib=lib) == want_i
+    for kk in ks[:12]:
+        assert oracle.corank_count(int(kk), A, B, lib=lib) == ((int(kk) + 1) // 2 if kk <= 2 * n else int(kk) - n)
+
+
+def check_pairs_ties_closed_form(lib, scale_log2=10):
+    """Heavy-tie pairs workload: for every key v in order, C holds all of A's
+    entries with key v (values = their A positions, ascending) and then all
+    of B's (values = 1<<31 | B positions, ascending)."""
+    d = synth.make_host("pairs_ties", scale_log2)
+    ka, va, kb, vb = d["keysA"], d["valsA"], d["keysB"], d["valsB"]
+    kc, vc = oracle.merge_pairs_u32(ka, va, kb, vb, lib=lib)
+    want_k, want_v = [], []
+    pa = pb = 0
+    for v in range(16):
+        ca = int(np.count_nonzero(ka == v))
+        cb = int(np.count_nonzero(kb == v))
+        want_k += [v] * (ca + cb)
+        want_v += list(range(pa, pa + ca)) + [(1 << 31) | p for p in range(pb, pb + cb)]
+        pa += ca
+        pb += cb
+    assert np.array_equal(kc, np.array(want_k, dtype=np.uint32))
+    assert np.array_equal(vc, np.array(want_v, dtype=np.uint32))
+
+
+def check_invariants_random(lib, trials=40, seed=5):
+    """Nondecreasing output, permutation of the inputs, A-first ties, and
+    i + j = k with the acceptance test at every split, on random inputs."""
+    rng = np.random.default_rng(seed)
+    for t in range(trials):
+        m = int(rng.integers(0, 300))
+        n = int(rng.integers(0, 300))
+        span = int(rng.choice([3, 50, 1 << 31]))
+        A = np.sort(rng.integers(-span, span, m)).astype(np.int32)
+        B = np.sort(rng.integers(-span, span, n)).astype(np.int32)
+        C = oracle.merge_i32(A, B, lib=lib)
+        assert np.all(np.diff(C.astype(np.int64)) >= 0)
+        assert np.array_equal(np.sort(C), np.sort(np.concatenate([A, B])))
+        for k in range(0, m + n + 1, max(1, (m + n) // 17)):
+            i = oracle.corank_pages(k, A, B, lib=lib)
+            j = k - i
+            assert max(0, k - n) <= i <= min(k, m)
+            assert i == 0 or j == n or A[i - 1] <= B[j]
+            assert j == 0 or i == m or B[j - 1] < A[i]
+            assert i == oracle.corank_count(k, A, B, lib=lib)
+        va = np.arange(m, dtype=np.uint32)
+        vb = np.arange(n, dtype=np.uint32) | np.uint32(1 << 31)
+        kc, vc = oracle.merge_pairs_u32(A.view(np.uint32) ^ np.uint32(1 << 31), va,
+                                        B.view(np.uint32) ^ np.uint32(1 << 31), vb, lib=lib)
+        # within each run of equal keys: every A tag before every B tag, each ascending
+        for key in np.unique(kc):
+            vals = vc[kc == key]
+            tags = vals >> np.uint32(31)
+            assert np.all(np.diff(tags.astype(np.int64)) >= 0)
+            assert np.all(np.diff((vals[tags == 0]).astype(np.int64)) > 0)
+            assert np.all(np.diff((vals[tags == 1] & np.uint32(0x7FFFFFFF)).astype(np.int64)) > 0)
+        # flipping the sign bit maps int32 order onto uint32 order
+        assert np.array_equal((kc ^ np.uint32(1 << 31)).view(np.int32), C)
+
+
+def check_merge_sort(lib, seed=9):
+    """O4 against numpy's stable argsort (a library stable sort), including
+    heavy ties, and the sort definition itself (nondecreasing permutation)."""
+    rng = np.random.default_rng(seed)
+    for n, hi in [(0, 10), (1, 10), (2, 3), (7, 3), (100, 5), (1000, 1 << 32), (4099, 40)]:
+        keys = rng.integers(0, hi, n, dtype=np.uint64).astype(np.uint32)
+        vals = np.arange(n, dtype=np.uint32)
+        sk, sv = oracle.merge_sort_pairs_u32(keys, vals, lib=lib)
+        order = np.argsort(keys, kind="stable")
+        assert np.array_equal(sk, keys[order])
+        assert np.array_equal(sv, vals[order])
+        assert np.all(np.diff(sk.astype(np.int64)) >= 0)
+
+
+ALL_CHECKS = [
+    check_worked_example,
+    check_tie_case,
+    check_brute_force,
+    check_evens_odds_closed_form,
+    check_pairs_ties_closed_form,
+    check_invariants_random,
+    check_merge_sort,
+]
+
+
+# ------------------------------------------------------------------ tests --
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda f: f.__name__)
+def test_oracle_pin(check, oracle_lib):
+    check(oracle_lib)
+
+
+def test_evens_odds_closed_form_full_size(oracle_lib):
+    """The full evens/odds workload (4,194,915 outputs), not a scaled copy."""
+    check_evens_odds_closed_form(oracle_lib, scale_log2=0)
+
+
+def test_pairs_ties_closed_form_larger(oracle_lib):
+    check_pairs_ties_closed_form(oracle_lib, scale_log2=6)
+
+
+def test_corank_step_bound(oracle_lib):
+    """The pages' loop takes at most bitlength(min(m, n)) + 1 iterations
+    (the interval starts no wider than min(m, n) and halves each step; the
+    extra row is the accepting one)."""
+    d = synth.make_host("evens_odds", 6)
+    A, B = d["A"], d["B"]
+    bound = int(min(A.size, B.size)).bit_length() + 1
+    for k in [0, 1, 5, 1000, A.size, A.size + B.size]:
+        _, rows = oracle.corank_pages(k, A, B, trace=True, lib=oracle_lib)
+        assert len(rows) <= bound
+
+
+def test_merge_sort_matches_python_sorted(oracle_lib):
+    rng = np.random.default_rng(3)
+    keys = rng.integers(0, 7, 257).astype(np.uint32)
+    vals = np.arange(257, dtype=np.uint32)
+    sk, sv = oracle.merge_sort_pairs_u32(keys, vals, lib=oracle_lib)
+    want = sorted(zip(keys.tolist(), vals.tolist()), key=lambda t: t[0])
+    assert list(zip(sk.tolist(), sv.tolist())) == want
