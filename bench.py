@@ -1,0 +1,529 @@
+#!/usr/bin/env python3
+"""Benchmark of the stable co-rank merge on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload: int32 merge of two sorted uniform full-range arrays,
+m = n = 2^28 (2^29 outputs, 2 GiB read + 2 GiB written per merge).  One step
+= one om_merge_i32 call (partition kernel + tile-merge kernel) on inputs
+already resident in HBM.  Prints ONE JSON line on rank 0.
+
+  value      merged elements/s over the K timed steps (CUDA events on the
+             launching stream; max over ranks for N > 1, times N replicas)
+  roofline   the tile-merge kernel: algorithmic bytes per launch
+             ((m+n) * (4 read + 4 written)) / its mean launch time (events
+             around each launch), against the measured HBM copy peak
+  e2e        the same metric with the host<->device copies inside the timed
+             region: pinned host A, B -> device, merge, device C -> pinned host
+  cpu_baseline  the CPU oracle (single thread) on the same workload
+  clocks     nvidia-smi samples taken during the timed region
+
+--impl reference times the CPU oracle alone on a bounded sample per step.
+N > 1 runs independent replicas (the merge needs no exchange across GPUs in
+this configuration), one process per GPU under torchrun.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "merged elements/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "elements/s"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "uniform": "int32 merge at bandwidth scale: A, B = 2^28 sorted uniform full-range int32 each",
+    "evens_odds": "int32 merge, A = evens (2^21+611), B = odds (2^21)",
+    "skewed": "int32 merge, A = 2^28 sorted full-range, B = 2^10 sorted in [-2^20, 2^20]",
+    "pairs_ties": "uint32 key+value merge, m = n = 2^24, keys in [0,16)",
+    "sort": "stable merge sort of 2^26 uint32 keys with index payload",
+}
+
+# Source files whose change invalidates a recorded ncu traffic figure.
+KERNEL_SOURCES = [
+    "ordered_merge_gb300/csrc/merge_kernels.cuh",
+    "ordered_merge_gb300/csrc/om_ptx.cuh",
+    "ordered_merge_gb300/csrc/api.cu",
+]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tile_merge_uniform_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes of the tile-merge kernel from a committed ncu
+    summary, or None when there is none or the kernel changed since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("workload") != workload or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("traffic_bytes_per_launch")
+
+
+def load_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of x over ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="om_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", str(self.period_ms)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        # samples under load: power above the midpoint of the observed range
+        if power:
+            thr = (min(power) + max(power)) / 2
+            loaded = [num(r[1]) for r in rows if num(r[3]) is not None and num(r[3]) >= thr and num(r[1])]
+        else:
+            loaded = sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {
+            "sm_mhz": statistics.median(loaded or sm) if (loaded or sm) else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": reasons,
+            "samples": len(rows),
+            "power_w_max": max(power) if power else None,
+        }
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_rate(A, B, budget_s: float = 12.0, max_reps: int = 5):
+    """Elements/s of the single-thread oracle merge on host arrays A, B."""
+    import oracle
+
+    lib = oracle.load()
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_reps:
+        t0 = time.perf_counter()
+        oracle.merge_i32(A, B, lib=lib)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    best = statistics.median(times)
+    return (A.size + B.size) / best, len(times), best
+
+
+# ------------------------------------------------------------- our arm --
+
+def bench_ours(args):
+    import numpy as np
+    import torch
+
+    import ordered_merge_gb300 as om
+    import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+
+    wl = args.workload
+    d = synth.make_device(wl, device)
+    stream = torch.cuda.current_stream(device)
+
+    if wl in ("uniform", "evens_odds", "skewed"):
+        A, B = d["A"], d["B"]
+        m, n = A.numel(), B.numel()
+        total = m + n
+        bytes_per_elem = 8
+        C = torch.empty(total, dtype=torch.int32, device=device)
+        step = lambda: om.merge_i32(A, B, C)
+        units_per_step = total
+    elif wl == "pairs_ties":
+        ka, va, kb, vb = d["keysA"], d["valsA"], d["keysB"], d["valsB"]
+        m, n = ka.numel(), kb.numel()
+        total = m + n
+        bytes_per_elem = 16
+        kc = torch.empty(total, dtype=torch.int32, device=device)
+        vc = torch.empty_like(kc)
+        step = lambda: om.merge_pairs_u32(ka, va, kb, vb, kc, vc)
+        units_per_step = total
+    else:  # sort: restore the unsorted input before each step (outside the timed events)
+        keys0, vals0 = d["keys"], d["vals"]
+        m, n = keys0.numel(), 0
+        total = m
+        bytes_per_elem = 16
+        keys, vals = keys0.clone(), vals0.clone()
+        step = None
+        units_per_step = total
+
+    # ---- warm-up, then K timed steps
+    if step is not None:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(device)
+        if om.device_error() != 0:
+            raise RuntimeError("device error during warm-up")
+        barrier(world, device)
+        torch.cuda.synchronize(device)
+        om.om_trace_reset()
+        om.om_trace_enable(True)
+        launches0 = om.om_launch_count()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            ev0.record(stream)
+            for _ in range(args.steps):
+                step()
+            ev1.record(stream)
+            torch.cuda.synchronize(device)
+        launches = om.om_launch_count() - launches0
+        om.om_trace_enable(False)
+        ms = ev0.elapsed_time(ev1)
+    else:
+        for _ in range(args.warmup):
+            keys.copy_(keys0)
+            vals.copy_(vals0)
+            om.merge_sort_u32(keys, vals)
+        torch.cuda.synchronize(device)
+        barrier(world, device)
+        om.om_trace_reset()
+        om.om_trace_enable(True)
+        launches0 = om.om_launch_count()
+        ms = 0.0
+        with ClockSampler(local) as clk:
+            for _ in range(args.steps):
+                keys.copy_(keys0)
+                vals.copy_(vals0)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                om.merge_sort_u32(keys, vals)
+                e1.record(stream)
+                e1.synchronize()
+                ms += e0.elapsed_time(e1)
+        launches = om.om_launch_count() - launches0
+        om.om_trace_enable(False)
+    if om.device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+    clocks = clk.summary()
+
+    ms_max = reduce_max(ms, world, device)
+    ms_per_step = ms_max / args.steps
+    value = world * units_per_step * args.steps / (ms_max / 1e3)
+
+    tm_launches, tm_ms = om.om_trace_read(om.KIND_TILE_MERGE)
+    p_launches, p_ms = om.om_trace_read(om.KIND_PARTITION)
+    bs_launches, bs_ms = om.om_trace_read(om.KIND_BLOCK_SORT)
+    peak, peak_src = load_peak()
+    if wl == "sort":
+        # dominant kernel: the late-pass tile merge; per launch it moves one
+        # pass of n elements: 8 B read + 8 B written
+        alg_bytes = total * 16
+    else:
+        alg_bytes = total * bytes_per_elem
+    tm_avg_ms = tm_ms / tm_launches if tm_launches else float("nan")
+    achieved = alg_bytes / (tm_avg_ms / 1e3) / 1e9 if tm_launches else None
+    traffic = recorded_traffic(wl)
+    roofline = {
+        "kernel": "tile_merge_kernel",
+        "bound": "hbm",
+        "achieved": round(achieved, 1) if achieved else None,
+        "peak": peak,
+        "peak_source": peak_src,
+        "unit": "GB/s",
+        "frac": round(achieved / peak, 4) if achieved else None,
+        "traffic": traffic,
+        "alg_bytes_per_launch": alg_bytes,
+        "mean_launch_ms": round(tm_avg_ms, 5),
+        "launches": tm_launches,
+    }
+    kernel_share = {
+        "tile_merge_ms": round(tm_ms, 4),
+        "partition_ms": round(p_ms, 4),
+        "block_sort_ms": round(bs_ms, 4),
+    }
+
+    # ---- end to end through the C-ABI call with host buffers
+    e2e = None
+    if wl in ("uniform", "evens_odds", "skewed") and args.e2e_steps > 0:
+        hA = torch.empty(m, dtype=torch.int32, pin_memory=True)
+        hB = torch.empty(n, dtype=torch.int32, pin_memory=True)
+        hC = torch.empty(total, dtype=torch.int32, pin_memory=True)
+        hA.copy_(A)
+        hB.copy_(B)
+        dA, dB = torch.empty_like(A), torch.empty_like(B)
+
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            om.merge_i32(dA, dB, C)
+            hC.copy_(C, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(world, device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        e_ms = reduce_max(e0.elapsed_time(e1), world, device)
+        e2e = {
+            "value": world * total * args.e2e_steps / (e_ms / 1e3),
+            "unit": UNIT,
+            "h2d_bytes_per_step": (m + n) * 4,
+            "d2h_bytes_per_step": total * 4,
+            "steps": args.e2e_steps,
+            "ms_per_step": e_ms / args.e2e_steps,
+        }
+        del dA, dB
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl in ("uniform", "evens_odds", "skewed"):
+        import oracle  # noqa: F401  (test infrastructure: the baseline leg only)
+
+        hA_np = A.cpu().numpy()
+        hB_np = B.cpu().numpy()
+        rate, reps, best = oracle_rate(hA_np, hB_np)
+        cpu = {
+            "value": rate,
+            "unit": UNIT,
+            "cores": 1,
+            "kind": "oracle",
+            "sample": f"the full workload ({total} outputs), median of {reps} single-thread oracle merges "
+                      f"({best:.2f} s each)",
+            "host_threads_available": os.cpu_count(),
+        }
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int32" if wl in ("uniform", "evens_odds", "skewed") else "u32",
+            "data": "synthetic (seeded SplitMix64, sorted on device)",
+            "config": {
+                "workload": WORKLOADS[wl],
+                "name": wl,
+                "m": m,
+                "n": n,
+                "l2": "inputs larger than L2 (no flush)" if total * 4 > 2 * 129e6 else
+                      "inputs smaller than L2: back-to-back steps may hit L2",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+            },
+            "achieved_gbs": round(units_per_step * (bytes_per_elem if wl != "sort" else 16) * args.steps
+                                  / (ms / 1e3) / 1e9, 1) if wl != "sort" else None,
+            "roofline": roofline,
+            "kernel_time_ms": kernel_share,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if line["achieved_gbs"] is not None:
+            line["pct_of_hbm_peak"] = round(100.0 * line["achieved_gbs"] / peak, 2)
+        print(json.dumps(line), flush=True)
+    barrier(world, device)
+
+
+# ------------------------------------------------------- reference arm --
+
+def bench_reference(args):
+    """The CPU oracle as it stands, timed on the host cores, on a bounded
+    sample of the same workload per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import synth
+
+    lib = oracle.load()
+    # per-step sample: same recipe, scaled so all K + W steps take ~60 s
+    budget_s = 60.0
+    rate_guess = 2.5e8
+    per_step = budget_s * rate_guess / max(1, args.steps + args.warmup)
+    scale = 0
+    total_full = sum(synth.sizes(args.workload if args.workload != "sort" else "uniform", 0))
+    while total_full >> scale > per_step and scale < 20:
+        scale += 1
+    wl = args.workload if args.workload in ("uniform", "evens_odds", "skewed") else "uniform"
+    d = synth.make_host(wl, scale_log2=scale)
+    A, B = d["A"], d["B"]
+    for _ in range(args.warmup):
+        oracle.merge_i32(A, B, lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.merge_i32(A, B, lib=lib)
+    dt = time.perf_counter() - t0
+    total = A.size + B.size
+    value = total * args.steps / dt
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic (seeded SplitMix64)",
+        "config": {"workload": WORKLOADS[wl], "name": wl, "m": int(A.size), "n": int(B.size),
+                   "sample_scale_log2": scale, "parallelism": "host CPU, 1 thread"},
+        "cpu_baseline": {
+            "value": value,
+            "unit": UNIT,
+            "cores": 1,
+            "kind": "oracle",
+            "sample": f"{wl} recipe scaled by 2^-{scale}: {total} outputs per step",
+        },
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default="uniform", choices=sorted(WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,140 @@
+/*
+ * ordmerge.h -- C ABI of the GB300 (sm_103a) stable co-rank merge library
+ * (libordmerge.so).
+ *
+ * Operation.  C = merge(A, B): the stable merge of two arrays that are each
+ * sorted nondecreasing.  When an element of A equals an element of B, the A
+ * element comes first.  The work is split by the co-rank function: for an
+ * output rank k, co_rank(k) is the i (with j = k - i) such that A[0..i) and
+ * B[0..j) are exactly the first k outputs, i.e. the unique i with
+ *     (i == 0 || j == n || A[i-1] <= B[j])  and  (j == 0 || i == m || B[j-1] < A[i]).
+ * Sources: "Co-rank Function 實作與 Basic Parallel Merge Kernel"
+ * (§Co-rank Function 定義與不變式, §Binary-Search Implementation, §Important on
+ * the asymmetric test); "Tiled 與 Circular Buffer Merge Kernel (Memory
+ * Coalescing)" (§Block-Level Co-Rank, §Circular Buffer Merge Kernel);
+ * "merge_path.cu" (coRank, mergeCpu); "排序 (Sorting) 練習題" (merge-sort
+ * stages, stable sort).
+ *
+ * Conventions for every call below.
+ *  - Array arguments are DEVICE pointers (memory the current CUDA device can
+ *    address: cudaMalloc, cudaMallocAsync, managed, or a torch CUDA tensor).
+ *    The caller owns them.  Element pointers must be 4-byte aligned; for
+ *    key/value calls, each value array must have the same address modulo 16
+ *    as its key array.  Output arrays must not overlap input arrays.
+ *  - Lengths are element counts (int64).  m = 0 or n = 0 is valid (the merge
+ *    is then a copy); m + n = 0 is a no-op.
+ *  - Inputs must be sorted nondecreasing (signed order for int32, unsigned for
+ *    uint32).  This is a precondition and is not checked; on unsorted input
+ *    the output is unspecified, but every kernel still terminates.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Merge and sort calls are asynchronous with respect to the
+ *    host: they validate, enqueue and return.  Errors raised while the
+ *    kernels run surface at the caller's next synchronisation, and in
+ *    om_device_error().
+ *  - Scratch (co-rank splitter arrays; the sort's second buffer) is taken
+ *    with cudaMallocAsync on `stream` and released with cudaFreeAsync on the
+ *    same stream, so it is stream-ordered; failure returns OM_ENOMEM.
+ *  - No call exits the process or prints.  A failing call returns a status.
+ */
+#ifndef ORDMERGE_H
+#define ORDMERGE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    OM_OK = 0,
+    OM_EINVAL = 1,  /* NULL pointer with a nonzero length, negative length,
+                       misaligned pointer, overlapping output */
+    OM_ERANGE = 2,  /* k outside [0, m + n], or m + n overflows */
+    OM_ENOMEM = 3,  /* stream-ordered scratch allocation failed */
+    OM_ECUDA = 4,   /* a CUDA runtime call or kernel launch failed */
+    OM_EDEVICE = 5  /* a kernel reported an error (om_device_error) */
+} om_status;
+
+/*
+ * co_rank(k) of A[0..m) and B[0..n): returns i in [max(0, k-n), min(k, m)];
+ * the caller derives j = k - i ("Co-rank Function 實作與 Basic Parallel Merge
+ * Kernel", §Co-rank Function 定義與不變式: the function returns i only).
+ * Runs one search on the device and waits for it: synchronous.  It is
+ * ordered after prior work on the legacy default stream only.  Returns the
+ * negated om_status (< 0) on error.
+ */
+int64_t om_corank_i32(int64_t k, const int32_t *A, int64_t m,
+                      const int32_t *B, int64_t n);
+
+/*
+ * Batched co-rank on the device: i_out[t] = co_rank(ks[t]) for t < count.
+ * ks and i_out are device arrays of int64 (each ks[t] in [0, m + n]; an
+ * out-of-range k is clamped into that interval).  Asynchronous on `stream`.
+ */
+om_status om_corank_i32_batch(const int64_t *ks, int64_t count,
+                              const int32_t *A, int64_t m,
+                              const int32_t *B, int64_t n,
+                              int64_t *i_out, void *stream);
+
+/*
+ * C[0 .. m+n) = stable merge of int32 A[0..m) and B[0..n); ties take A
+ * first.  Launches the partition kernel (one co-rank per output range) and
+ * the circular-buffer tile-merge kernel on `stream`.
+ */
+om_status om_merge_i32(const int32_t *A, int64_t m, const int32_t *B,
+                       int64_t n, int32_t *C, void *stream);
+
+/*
+ * Stable merge of (uint32 key, uint32 value) pairs, comparing keys only
+ * (unsigned order); each value travels with its key; ties take A first.
+ * Outputs keysC / valsC hold m + n elements.
+ */
+om_status om_merge_pairs_u32(const uint32_t *keysA, const uint32_t *valsA,
+                             int64_t m, const uint32_t *keysB,
+                             const uint32_t *valsB, int64_t n,
+                             uint32_t *keysC, uint32_t *valsC, void *stream);
+
+/*
+ * Stable sort of keys[0..n) (unsigned order), in place, carrying vals along
+ * (vals may be NULL for a keys-only sort).  Built only from merges: runs of
+ * 1024 are sorted in shared memory, then runs are merged pairwise, with many
+ * small merges per thread block in early passes and co-rank-split large
+ * merges in late passes ("排序 (Sorting) 練習題", merge-sort stages).
+ * Equal keys keep their input order.  Needs 4*n (8*n with vals) bytes of
+ * stream-ordered scratch.
+ */
+om_status om_merge_sort_u32(uint32_t *keys, uint32_t *vals, int64_t n,
+                            void *stream);
+
+/* Human-readable name of a status (static string). */
+const char *om_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error
+ * word on the current device.  Returns OM_OK, OM_EDEVICE when a kernel
+ * recorded an error (for example a shared-memory barrier wait that hit its
+ * time limit), or OM_ECUDA.  *detail (if not NULL) receives the raw word.
+ */
+om_status om_device_error(void *stream, uint32_t *detail);
+
+/* ---- tracing and counters (used by the benchmark) ---------------------- */
+
+/*
+ * With tracing on, every kernel launch is bracketed by two CUDA events on its
+ * stream.  om_trace_read synchronises those events and returns, for kernel
+ * kind `kind` (0 = partition, 1 = tile merge, 2 = block sort / small merge,
+ * 3 = co-rank batch), the number of launches and their summed duration in
+ * milliseconds since the last om_trace_reset.
+ */
+om_status om_trace_enable(int on);
+om_status om_trace_reset(void);
+om_status om_trace_read(int kind, int64_t *launches, double *total_ms);
+
+/* Number of kernels this library has launched since load. */
+uint64_t om_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ORDMERGE_H */

@@ -1,0 +1,216 @@
+"""Python binding of libordmerge.so, the GB300 stable co-rank merge library.
+
+Argument marshalling only: every function checks tensors, takes their device
+pointers and the current CUDA stream, and calls the C ABI declared in
+``include/ordmerge.h`` through ctypes.  All computation runs in the library's
+CUDA kernels; there is no CPU path.  PyTorch is used for device memory and
+streams.
+
+Import fails loudly if the library has not been built
+(``python -m ordered_merge_gb300.build`` or ``__graft_entry__.build()``).
+
+Functions carry the C names (``om_merge_i32`` ...) with unprefixed aliases
+(``merge_i32`` ...).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+OM_OK, OM_EINVAL, OM_ERANGE, OM_ENOMEM, OM_ECUDA, OM_EDEVICE = range(6)
+
+KIND_PARTITION, KIND_TILE_MERGE, KIND_BLOCK_SORT, KIND_CORANK = range(4)
+
+
+class OrdMergeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_status_string(status)} ({status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m ordered_merge_gb300.build` "
+            "(the merge has no CPU fallback)"
+        )
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.om_corank_i32.argtypes = [I64, P, I64, P, I64]
+    lib.om_corank_i32.restype = I64
+    lib.om_corank_i32_batch.argtypes = [P, I64, P, I64, P, I64, P, P]
+    lib.om_corank_i32_batch.restype = I32
+    lib.om_merge_i32.argtypes = [P, I64, P, I64, P, P]
+    lib.om_merge_i32.restype = I32
+    lib.om_merge_pairs_u32.argtypes = [P, P, I64, P, P, I64, P, P, P]
+    lib.om_merge_pairs_u32.restype = I32
+    lib.om_merge_sort_u32.argtypes = [P, P, I64, P]
+    lib.om_merge_sort_u32.restype = I32
+    lib.om_status_string.argtypes = [I32]
+    lib.om_status_string.restype = ctypes.c_char_p
+    lib.om_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.om_device_error.restype = I32
+    lib.om_trace_enable.argtypes = [I32]
+    lib.om_trace_enable.restype = I32
+    lib.om_trace_reset.argtypes = []
+    lib.om_trace_reset.restype = I32
+    lib.om_trace_read.argtypes = [I32, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)]
+    lib.om_trace_read.restype = I32
+    lib.om_launch_count.argtypes = []
+    lib.om_launch_count.restype = ctypes.c_uint64
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    """The ctypes handle of libordmerge.so (for direct C-ABI calls)."""
+    return _lib
+
+
+def _status_string(status: int) -> str:
+    return _lib.om_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != OM_OK:
+        raise OrdMergeError(status, what)
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr4(t, name: str):
+    """Device pointer of a contiguous CUDA tensor of 4-byte elements."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.element_size() != 4:
+        raise ValueError(f"{name} must have 4-byte elements (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr() if t.numel() else None
+
+
+def om_corank_i32(k: int, A, B) -> int:
+    """co_rank(k) of int32 device tensors A, B (synchronous); j = k - i."""
+    r = _lib.om_corank_i32(int(k), _ptr4(A, "A"), A.numel(), _ptr4(B, "B"), B.numel())
+    if r < 0:
+        raise OrdMergeError(int(-r), "om_corank_i32")
+    return int(r)
+
+
+def om_corank_i32_batch(ks, A, B, out=None, stream=None):
+    """i[t] = co_rank(ks[t]) for an int64 device tensor ks (asynchronous)."""
+    import torch
+
+    if ks.dtype != torch.int64 or not ks.is_cuda or not ks.is_contiguous():
+        raise ValueError("ks must be a contiguous int64 CUDA tensor")
+    if out is None:
+        out = torch.empty_like(ks)
+    _check(
+        _lib.om_corank_i32_batch(ks.data_ptr() if ks.numel() else None, ks.numel(), _ptr4(A, "A"), A.numel(),
+                                 _ptr4(B, "B"), B.numel(), out.data_ptr() if out.numel() else None,
+                                 _stream(stream)),
+        "om_corank_i32_batch",
+    )
+    return out
+
+
+def om_merge_i32(A, B, C=None, stream=None):
+    """C = stable merge of sorted int32 device tensors A and B (ties: A first)."""
+    import torch
+
+    if C is None:
+        C = torch.empty(A.numel() + B.numel(), dtype=torch.int32, device=A.device)
+    if C.numel() != A.numel() + B.numel():
+        raise ValueError("C must hold len(A) + len(B) elements")
+    _check(
+        _lib.om_merge_i32(_ptr4(A, "A"), A.numel(), _ptr4(B, "B"), B.numel(), _ptr4(C, "C"), _stream(stream)),
+        "om_merge_i32",
+    )
+    return C
+
+
+def om_merge_pairs_u32(keysA, valsA, keysB, valsB, keysC=None, valsC=None, stream=None):
+    """Stable merge of (uint32 key, uint32 value) pairs; keys compared unsigned.
+
+    uint32 data may be carried in int32 tensors (bits are reinterpreted).
+    """
+    import torch
+
+    m, n = keysA.numel(), keysB.numel()
+    if valsA.numel() != m or valsB.numel() != n:
+        raise ValueError("each value array must match its key array")
+    if keysC is None:
+        keysC = torch.empty(m + n, dtype=keysA.dtype, device=keysA.device)
+    if valsC is None:
+        valsC = torch.empty(m + n, dtype=valsA.dtype, device=valsA.device)
+    if keysC.numel() != m + n or valsC.numel() != m + n:
+        raise ValueError("outputs must hold len(A) + len(B) elements")
+    _check(
+        _lib.om_merge_pairs_u32(_ptr4(keysA, "keysA"), _ptr4(valsA, "valsA"), m, _ptr4(keysB, "keysB"),
+                                _ptr4(valsB, "valsB"), n, _ptr4(keysC, "keysC"), _ptr4(valsC, "valsC"),
+                                _stream(stream)),
+        "om_merge_pairs_u32",
+    )
+    return keysC, valsC
+
+
+def om_merge_sort_u32(keys, vals=None, stream=None):
+    """Stable in-place sort of uint32 keys (unsigned order), carrying vals."""
+    n = keys.numel()
+    if vals is not None and vals.numel() != n:
+        raise ValueError("vals must match keys")
+    _check(
+        _lib.om_merge_sort_u32(_ptr4(keys, "keys"), _ptr4(vals, "vals") if vals is not None else None, n,
+                               _stream(stream)),
+        "om_merge_sort_u32",
+    )
+    return keys, vals
+
+
+def om_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word."""
+    w = ctypes.c_uint32(0)
+    st = _lib.om_device_error(_stream(stream), ctypes.byref(w))
+    if st not in (OM_OK, OM_EDEVICE):
+        raise OrdMergeError(st, "om_device_error")
+    return int(w.value)
+
+
+def om_trace_enable(on: bool = True):
+    _check(_lib.om_trace_enable(1 if on else 0), "om_trace_enable")
+
+
+def om_trace_reset():
+    _check(_lib.om_trace_reset(), "om_trace_reset")
+
+
+def om_trace_read(kind: int):
+    """(launches, total_ms) of one kernel kind since the last reset."""
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check(_lib.om_trace_read(kind, ctypes.byref(n), ctypes.byref(ms)), "om_trace_read")
+    return int(n.value), float(ms.value)
+
+
+def om_launch_count() -> int:
+    return int(_lib.om_launch_count())
+
+
+corank_i32 = om_corank_i32
+corank_i32_batch = om_corank_i32_batch
+merge_i32 = om_merge_i32
+merge_pairs_u32 = om_merge_pairs_u32
+merge_sort_u32 = om_merge_sort_u32
+device_error = om_device_error

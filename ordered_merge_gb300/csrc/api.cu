@@ -1,0 +1,438 @@
+// C ABI of the stable co-rank merge library (declared in include/ordmerge.h):
+// argument checks, stream-ordered scratch, kernel launches, the merge-sort
+// pass schedule, tracing and the device error word.
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "merge_kernels.cuh"
+#include "ordmerge.h"
+#include "sort_kernels.cuh"
+
+namespace om {
+
+// Kernel configurations.
+//  merge: 128 threads x 15 outputs = 1920 outputs per sub-tile; 4096-element
+//         rings per side refilled in 512-element (2 KB) chunks.
+using MergeCfg = TileCfg<128, 15, 12, 9>;
+//  sort: runs of 1024 from a 128 x 8 block sort; early passes merge whole
+//        pairs of runs inside 256 x 16 = 4096-element tiles; later passes use
+//        the partition + tile-merge kernels on each pair of runs.
+using RunSortCfg = BlockSortCfg<128, 8>;
+using SmallMergeCfg = BlockSortCfg<256, 16>;
+constexpr int kRunLen = RunSortCfg::TILE;  // 1024
+
+enum KernelKind { kKindPartition = 0, kKindTileMerge = 1, kKindBlockSort = 2, kKindCorank = 3, kNumKinds = 4 };
+
+// ------------------------------------------------------------ device state --
+
+static __device__ uint32_t g_error_word;
+static __device__ int64_t g_corank_slot;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    uint32_t* err = nullptr;
+    int64_t* corank_slot = nullptr;
+};
+
+static std::mutex g_mu;
+static DeviceState g_devices[128];
+static std::mutex g_corank_mu;
+static std::atomic<uint64_t> g_launches{0};
+
+template <typename F>
+static cudaError_t set_smem(F* kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// Per-device set-up, once: SM count, addresses of the library's device
+// words, shared-memory limits of the kernels.
+static om_status device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return OM_ECUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& d = g_devices[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return OM_ECUDA;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_error_word) != cudaSuccess) return OM_ECUDA;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.corank_slot), g_corank_slot) != cudaSuccess)
+            return OM_ECUDA;
+        cudaError_t e = cudaSuccess;
+        e = e ? e : set_smem(tile_merge_kernel<MergeCfg, int32_t, false>, TileSmem<MergeCfg, false>::total);
+        e = e ? e : set_smem(tile_merge_kernel<MergeCfg, uint32_t, false>, TileSmem<MergeCfg, false>::total);
+        e = e ? e : set_smem(tile_merge_kernel<MergeCfg, uint32_t, true>, TileSmem<MergeCfg, true>::total);
+        e = e ? e : set_smem(block_sort_kernel<RunSortCfg, true>, block_sort_smem_bytes<RunSortCfg, true>());
+        e = e ? e : set_smem(block_sort_kernel<RunSortCfg, false>, block_sort_smem_bytes<RunSortCfg, false>());
+        e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, true>, block_sort_smem_bytes<SmallMergeCfg, true>());
+        e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, false>, block_sort_smem_bytes<SmallMergeCfg, false>());
+        if (e != cudaSuccess) return OM_ECUDA;
+        d.ready = true;
+    }
+    *out = &d;
+    return OM_OK;
+}
+
+// ----------------------------------------------------------------- tracing --
+
+struct TraceRec {
+    int kind;
+    cudaEvent_t e0, e1;
+};
+
+static std::mutex g_trace_mu;
+static bool g_trace_on = false;
+static std::vector<TraceRec> g_trace_recs;
+static std::vector<cudaEvent_t> g_event_pool;
+static int64_t g_trace_launches[kNumKinds];
+static double g_trace_ms[kNumKinds];
+
+static cudaEvent_t pool_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Launches through `launch` (a callable issuing exactly one kernel), counting
+// it and, with tracing on, bracketing it with events on `stream`.
+template <typename F>
+static cudaError_t traced(int kind, cudaStream_t stream, F&& launch) {
+    TraceRec rec{kind, nullptr, nullptr};
+    bool on;
+    {
+        std::lock_guard<std::mutex> lk(g_trace_mu);
+        on = g_trace_on;
+        if (on) {
+            rec.e0 = pool_event();
+            rec.e1 = pool_event();
+        }
+    }
+    if (on) cudaEventRecord(rec.e0, stream);
+    launch();
+    cudaError_t e = cudaGetLastError();
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (on) {
+        cudaEventRecord(rec.e1, stream);
+        std::lock_guard<std::mutex> lk(g_trace_mu);
+        g_trace_recs.push_back(rec);
+    }
+    return e;
+}
+
+static void trace_collect_locked() {
+    for (const TraceRec& r : g_trace_recs) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.e1) == cudaSuccess && cudaEventElapsedTime(&ms, r.e0, r.e1) == cudaSuccess) {
+            g_trace_launches[r.kind] += 1;
+            g_trace_ms[r.kind] += ms;
+        }
+        g_event_pool.push_back(r.e0);
+        g_event_pool.push_back(r.e1);
+    }
+    g_trace_recs.clear();
+}
+
+// ------------------------------------------------------------------ helpers --
+
+static bool misaligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) != 0; }
+
+static bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+    if (na <= 0 || nb <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), a1 = a0 + (uintptr_t)na * 4;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + (uintptr_t)nb * 4;
+    return a0 < b1 && b0 < a1;
+}
+
+static int64_t env_int(const char* name, int64_t fallback) {
+    const char* s = std::getenv(name);
+    if (s == nullptr || *s == 0) return fallback;
+    char* end = nullptr;
+    const long long v = std::strtoll(s, &end, 10);
+    return (end != s && v > 0) ? (int64_t)v : fallback;
+}
+
+// Sub-tiles per CTA output range: long ranges amortise each CTA's start-up
+// (the first chunks' latency), but there must be enough ranges to fill every
+// SM several times over.  OM_SUBTILES_PER_RANGE overrides (tuning).
+static int64_t subtiles_per_range(int64_t subtiles, int sm_count) {
+    int64_t s = subtiles / ((int64_t)sm_count * 32);
+    if (s < 1) s = 1;
+    if (s > 64) s = 64;
+    return env_int("OM_SUBTILES_PER_RANGE", s);
+}
+
+static om_status cuda_fail(cudaError_t e) {
+    return e == cudaErrorMemoryAllocation ? OM_ENOMEM : OM_ECUDA;
+}
+
+// Partition + tile-merge launches for one geometry (split has nranges + 1
+// slots of scratch).
+template <typename K, bool V>
+static cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const DeviceState* d, cudaStream_t st) {
+    using Smem = TileSmem<MergeCfg, V>;
+    const unsigned pgrid = (unsigned)((g.nranges + 127) / 128);
+    cudaError_t e = traced(kKindPartition, st, [&] { partition_kernel<K, V><<<pgrid, 128, 0, st>>>(g, split); });
+    if (e != cudaSuccess) return e;
+    return traced(kKindTileMerge, st, [&] {
+        tile_merge_kernel<MergeCfg, K, V><<<(unsigned)g.nranges, MergeCfg::NT, Smem::total, st>>>(g, split, d->err);
+    });
+}
+
+template <typename K, bool V>
+static om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, const uint32_t* bv,
+                            int64_t n, K* ck, uint32_t* cv, cudaStream_t st) {
+    DeviceState* d = nullptr;
+    om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    const int64_t total = m + n;
+    const int64_t subtiles = (total + MergeCfg::T - 1) / MergeCfg::T;
+    const int64_t range_len = subtiles_per_range(subtiles, d->sm_count) * MergeCfg::T;
+    const int64_t nranges = (total + range_len - 1) / range_len;
+    if (nranges > 0x7fffffff) return OM_ERANGE;
+    MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
+    int64_t* split = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&split), (size_t)(nranges + 1) * 8, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return OM_ENOMEM;
+    }
+    e = launch_merge<K, V>(g, split, d, st);
+    cudaError_t ef = cudaFreeAsync(split, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ef == cudaSuccess ? OM_OK : OM_ECUDA;
+}
+
+template <bool V>
+static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream_t st) {
+    DeviceState* d = nullptr;
+    om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+
+    // Pass schedule.  Run sort to kRunLen, then one pass per doubling.
+    int passes = 0;
+    for (int64_t r = kRunLen; r < n; r *= 2) ++passes;
+    const int64_t subtiles = (n + MergeCfg::T - 1) / MergeCfg::T;
+    const int64_t range_len = subtiles_per_range(subtiles, d->sm_count) * MergeCfg::T;
+    // splitter slots for the largest late pass: ranges of every pair, plus one
+    const int64_t max_ranges = (n + range_len - 1) / range_len + (n + 2 * kRunLen - 1) / (2 * kRunLen) + 1;
+
+    uint32_t* tk = nullptr;
+    uint32_t* tv = nullptr;
+    int64_t* split = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (passes > 0) {
+        e = cudaMallocAsync(reinterpret_cast<void**>(&tk), (size_t)n * 4, st);
+        if (e == cudaSuccess && V) e = cudaMallocAsync(reinterpret_cast<void**>(&tv), (size_t)n * 4, st);
+        if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&split), (size_t)max_ranges * 8, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            if (tk) cudaFreeAsync(tk, st);
+            if (tv) cudaFreeAsync(tv, st);
+            return OM_ENOMEM;
+        }
+    }
+    // The run sort writes where the pass count's parity makes the last pass
+    // land back in keys / vals.
+    uint32_t* src_k = (passes % 2 == 0) ? keys : tk;
+    uint32_t* src_v = (passes % 2 == 0) ? vals : tv;
+    uint32_t* dst_k = (passes % 2 == 0) ? tk : keys;
+    uint32_t* dst_v = (passes % 2 == 0) ? tv : vals;
+
+    {
+        const unsigned grid = (unsigned)((n + RunSortCfg::TILE - 1) / RunSortCfg::TILE);
+        e = traced(kKindBlockSort, st, [&] {
+            block_sort_kernel<RunSortCfg, V><<<grid, RunSortCfg::NT, block_sort_smem_bytes<RunSortCfg, V>(), st>>>(
+                keys, vals, src_k, src_v, n, 1, kRunLen);
+        });
+    }
+    for (int64_t r = kRunLen; e == cudaSuccess && r < n; r *= 2) {
+        if (2 * r <= SmallMergeCfg::TILE) {
+            // early pass: each CTA merges whole pairs of runs inside its tile
+            const unsigned grid = (unsigned)((n + SmallMergeCfg::TILE - 1) / SmallMergeCfg::TILE);
+            e = traced(kKindBlockSort, st, [&] {
+                block_sort_kernel<SmallMergeCfg, V>
+                    <<<grid, SmallMergeCfg::NT, block_sort_smem_bytes<SmallMergeCfg, V>(), st>>>(
+                        src_k, src_v, dst_k, dst_v, n, (int)r, (int)(2 * r));
+            });
+        } else {
+            // late pass: co-rank split of each pair of runs into output ranges
+            const int64_t npairs = (n + 2 * r - 1) / (2 * r);
+            const int64_t rps = (2 * r + range_len - 1) / range_len;
+            MergeGeom<uint32_t> g{src_k, src_v, nullptr, nullptr, dst_k, dst_v, n, 0, r, range_len, rps,
+                                  npairs * rps};
+            if (g.nranges + 1 > max_ranges || g.nranges > 0x7fffffff) {
+                e = cudaErrorInvalidValue;
+                break;
+            }
+            e = launch_merge<uint32_t, V>(g, split, d, st);
+        }
+        uint32_t* t;
+        t = src_k; src_k = dst_k; dst_k = t;
+        t = src_v; src_v = dst_v; dst_v = t;
+    }
+    if (passes > 0) {
+        cudaFreeAsync(split, st);
+        cudaFreeAsync(tk, st);
+        if (V) cudaFreeAsync(tv, st);
+    }
+    return e == cudaSuccess ? OM_OK : cuda_fail(e);
+}
+
+__global__ void corank_one_kernel(int64_t k, const int32_t* A, int64_t m, const int32_t* B, int64_t n,
+                                  int64_t* out) {
+    *out = corank_global(k, A, m, B, n);
+}
+
+}  // namespace om
+
+using namespace om;
+
+extern "C" {
+
+int64_t om_corank_i32(int64_t k, const int32_t* A, int64_t m, const int32_t* B, int64_t n) {
+    if (m < 0 || n < 0 || (m > 0 && A == nullptr) || (n > 0 && B == nullptr) || misaligned4(A) || misaligned4(B))
+        return -(int64_t)OM_EINVAL;
+    if (m > INT64_MAX - n || k < 0 || k > m + n) return -(int64_t)OM_ERANGE;
+    if (m == 0 || n == 0) return k < m ? k : m;  // the split is forced
+    DeviceState* d = nullptr;
+    om_status s = device_state(&d);
+    if (s != OM_OK) return -(int64_t)s;
+    std::lock_guard<std::mutex> lk(g_corank_mu);
+    cudaError_t e = traced(kKindCorank, (cudaStream_t)0,
+                           [&] { corank_one_kernel<<<1, 1, 0, 0>>>(k, A, m, B, n, d->corank_slot); });
+    if (e != cudaSuccess) return -(int64_t)OM_ECUDA;
+    int64_t i = -1;
+    if (cudaMemcpy(&i, d->corank_slot, sizeof(i), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return -(int64_t)OM_ECUDA;
+    return i;
+}
+
+om_status om_corank_i32_batch(const int64_t* ks, int64_t count, const int32_t* A, int64_t m, const int32_t* B,
+                              int64_t n, int64_t* i_out, void* stream) {
+    if (count < 0 || m < 0 || n < 0) return OM_EINVAL;
+    if (count == 0) return OM_OK;
+    if (ks == nullptr || i_out == nullptr || (m > 0 && A == nullptr) || (n > 0 && B == nullptr) ||
+        misaligned4(A) || misaligned4(B))
+        return OM_EINVAL;
+    if (m > INT64_MAX - n) return OM_ERANGE;
+    DeviceState* d = nullptr;
+    om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    const unsigned grid = (unsigned)((count + 127) / 128);
+    cudaError_t e = traced(kKindCorank, st,
+                           [&] { corank_batch_kernel<int32_t><<<grid, 128, 0, st>>>(ks, count, A, m, B, n, i_out); });
+    return e == cudaSuccess ? OM_OK : OM_ECUDA;
+}
+
+om_status om_merge_i32(const int32_t* A, int64_t m, const int32_t* B, int64_t n, int32_t* C, void* stream) {
+    if (m < 0 || n < 0) return OM_EINVAL;
+    if (m > INT64_MAX - n) return OM_ERANGE;
+    const int64_t total = m + n;
+    if (total == 0) return OM_OK;
+    if ((m > 0 && A == nullptr) || (n > 0 && B == nullptr) || C == nullptr) return OM_EINVAL;
+    if (misaligned4(A) || misaligned4(B) || misaligned4(C)) return OM_EINVAL;
+    if (overlaps(C, total, A, m) || overlaps(C, total, B, n)) return OM_EINVAL;
+    return merge_impl<int32_t, false>(A, nullptr, m, B, nullptr, n, C, nullptr, (cudaStream_t)stream);
+}
+
+om_status om_merge_pairs_u32(const uint32_t* keysA, const uint32_t* valsA, int64_t m, const uint32_t* keysB,
+                             const uint32_t* valsB, int64_t n, uint32_t* keysC, uint32_t* valsC, void* stream) {
+    if (m < 0 || n < 0) return OM_EINVAL;
+    if (m > INT64_MAX - n) return OM_ERANGE;
+    const int64_t total = m + n;
+    if (total == 0) return OM_OK;
+    if ((m > 0 && (keysA == nullptr || valsA == nullptr)) || (n > 0 && (keysB == nullptr || valsB == nullptr)) ||
+        keysC == nullptr || valsC == nullptr)
+        return OM_EINVAL;
+    const void* ptrs[6] = {keysA, valsA, keysB, valsB, keysC, valsC};
+    for (const void* p : ptrs)
+        if (misaligned4(p)) return OM_EINVAL;
+    auto phase = [](const void* p) { return reinterpret_cast<uintptr_t>(p) & 15; };
+    if ((m > 0 && phase(keysA) != phase(valsA)) || (n > 0 && phase(keysB) != phase(valsB)) ||
+        phase(keysC) != phase(valsC))
+        return OM_EINVAL;
+    if (overlaps(keysC, total, valsC, total)) return OM_EINVAL;
+    for (const void* out : {(const void*)keysC, (const void*)valsC})
+        if (overlaps(out, total, keysA, m) || overlaps(out, total, valsA, m) || overlaps(out, total, keysB, n) ||
+            overlaps(out, total, valsB, n))
+            return OM_EINVAL;
+    return merge_impl<uint32_t, true>(keysA, valsA, m, keysB, valsB, n, keysC, valsC, (cudaStream_t)stream);
+}
+
+om_status om_merge_sort_u32(uint32_t* keys, uint32_t* vals, int64_t n, void* stream) {
+    if (n < 0) return OM_EINVAL;
+    if (n <= 1) return OM_OK;
+    if (keys == nullptr || misaligned4(keys) || misaligned4(vals)) return OM_EINVAL;
+    if (n > (int64_t)1 << 40) return OM_ERANGE;
+    if (vals != nullptr) {
+        if ((reinterpret_cast<uintptr_t>(keys) & 15) != (reinterpret_cast<uintptr_t>(vals) & 15)) return OM_EINVAL;
+        if (overlaps(keys, n, vals, n)) return OM_EINVAL;
+        return sort_impl<true>(keys, vals, n, (cudaStream_t)stream);
+    }
+    return sort_impl<false>(keys, nullptr, n, (cudaStream_t)stream);
+}
+
+const char* om_status_string(int status) {
+    switch (status) {
+        case OM_OK: return "OM_OK";
+        case OM_EINVAL: return "OM_EINVAL: invalid argument (null, negative length, misaligned or overlapping)";
+        case OM_ERANGE: return "OM_ERANGE: k or a length out of range";
+        case OM_ENOMEM: return "OM_ENOMEM: scratch allocation failed";
+        case OM_ECUDA: return "OM_ECUDA: CUDA runtime or launch error";
+        case OM_EDEVICE: return "OM_EDEVICE: a kernel reported an error";
+        default: return "unknown status";
+    }
+}
+
+om_status om_device_error(void* stream, uint32_t* detail) {
+    DeviceState* d = nullptr;
+    om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return OM_ECUDA;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, d->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return OM_ECUDA;
+    if (w != 0 && cudaMemset(d->err, 0, sizeof(w)) != cudaSuccess) return OM_ECUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return OM_ECUDA;
+    if (detail) *detail = w;
+    return w ? OM_EDEVICE : OM_OK;
+}
+
+om_status om_trace_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace_on = on != 0;
+    return OM_OK;
+}
+
+om_status om_trace_reset(void) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    trace_collect_locked();
+    for (int k = 0; k < kNumKinds; ++k) {
+        g_trace_launches[k] = 0;
+        g_trace_ms[k] = 0.0;
+    }
+    return OM_OK;
+}
+
+om_status om_trace_read(int kind, int64_t* launches, double* total_ms) {
+    if (kind < 0 || kind >= kNumKinds) return OM_EINVAL;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    trace_collect_locked();
+    if (launches) *launches = g_trace_launches[kind];
+    if (total_ms) *total_ms = g_trace_ms[kind];
+    return OM_OK;
+}
+
+uint64_t om_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

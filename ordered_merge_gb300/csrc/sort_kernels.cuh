@@ -1,0 +1,178 @@
+// Block-level kernels of the stable merge sort on sm_103a.
+//
+// "排序 (Sorting) 練習題 (Practice - Sorting Foundations and Parallel Radix
+// Sort)", merge-sort stages: early stages have many small independent merges
+// (parallelism across merges: give different merges to different thread
+// blocks); late stages have few large merges (parallelism inside one merge:
+// cut it with the co-rank function).  The same page notes that sorting
+// networks are often fastest on short sequences.
+//
+// block_sort_kernel covers the early stages.  One CTA owns a tile of NT*VT
+// consecutive elements and, in shared memory, takes every run of length
+// run_from inside the tile to length run_to by pairwise merges:
+//  * run_from == 1: each thread first sorts its VT consecutive elements in
+//    registers with an odd-even transposition network that only swaps on
+//    strictly greater keys (so equal keys keep their order), then merges
+//    upward from runs of VT.
+//  * each merge step: thread t produces outputs [t*VT, t*VT + VT) of the
+//    merge its slice falls in (VT and the run lengths are powers of two, so a
+//    slice never straddles two merges), by a co-rank search in shared memory
+//    and a serial merge of VT outputs into registers (ties: earlier run
+//    first).
+// The kernel may run in place (out == in): a CTA reads its whole tile before
+// it writes any of it, and tiles do not overlap.
+// Shared memory indices are padded by one word per 32 so that the
+// register -> shared writes of VT consecutive elements per thread hit 32
+// distinct banks.
+#pragma once
+
+#include <cstdint>
+
+#include "om_ptx.cuh"
+
+namespace om {
+
+__device__ __forceinline__ int pad32(int x) { return x + (x >> 5); }
+
+template <int NT_, int VT_>
+struct BlockSortCfg {
+    static constexpr int NT = NT_;
+    static constexpr int VT = VT_;
+    static constexpr int TILE = NT * VT;
+    static constexpr int PADDED = TILE + TILE / 32;
+    static_assert((VT & (VT - 1)) == 0, "VT must be a power of two");
+    static_assert(TILE % 32 == 0, "tile is whole bank rows");
+};
+
+template <typename Cfg, bool V>
+constexpr size_t block_sort_smem_bytes() {
+    return (size_t)Cfg::PADDED * 4 * (V ? 2 : 1);
+}
+
+// co_rank(d) of A = s[pad(a0 + x)], x < m and B = s[pad(b0 + x)], x < n.
+__device__ __forceinline__ int corank_padded(int d, const uint32_t* s, int a0, int m, int b0, int n) {
+    int lo = d - n > 0 ? d - n : 0;
+    int hi = d < m ? d : m;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s[pad32(a0 + mid - 1)] <= s[pad32(b0 + d - mid)]) {
+            lo = mid;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    return lo;
+}
+
+template <typename Cfg, bool V>
+__global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const uint32_t* in_k, const uint32_t* in_v,
+                                                             uint32_t* out_k, uint32_t* out_v, int64_t n,
+                                                             int run_from, int run_to) {
+    constexpr int NT = Cfg::NT;
+    constexpr int VT = Cfg::VT;
+    constexpr int TILE = Cfg::TILE;
+    extern __shared__ __align__(16) uint32_t bsm[];
+    uint32_t* sk = bsm;
+    uint32_t* sv = V ? bsm + Cfg::PADDED : nullptr;
+
+    const int tid = threadIdx.x;
+    const int64_t base = (int64_t)blockIdx.x * TILE;
+    const int count = (int)((n - base) < TILE ? (n - base) : TILE);
+
+    for (int p = tid; p < count; p += NT) {
+        sk[pad32(p)] = in_k[base + p];
+        if (V) sv[pad32(p)] = in_v[base + p];
+    }
+    __syncthreads();
+
+    const int p0 = tid * VT;
+    uint32_t k[VT];
+    uint32_t v[VT];
+    int w = run_from;
+    if (run_from == 1) {
+        // Registers: elements past the tile end get the largest key and stay
+        // behind every real element (swaps need a strictly greater key).
+#pragma unroll
+        for (int i = 0; i < VT; ++i) {
+            const bool real = p0 + i < count;
+            k[i] = real ? sk[pad32(p0 + i)] : 0xFFFFFFFFu;
+            if (V) v[i] = real ? sv[pad32(p0 + i)] : 0u;
+        }
+#pragma unroll
+        for (int round = 0; round < VT; ++round) {
+#pragma unroll
+            for (int i = round & 1; i + 1 < VT; i += 2) {
+                if (k[i] > k[i + 1]) {
+                    const uint32_t tk = k[i];
+                    k[i] = k[i + 1];
+                    k[i + 1] = tk;
+                    if (V) {
+                        const uint32_t tv = v[i];
+                        v[i] = v[i + 1];
+                        v[i + 1] = tv;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < VT; ++i) {
+            if (p0 + i < count) {
+                sk[pad32(p0 + i)] = k[i];
+                if (V) sv[pad32(p0 + i)] = v[i];
+            }
+        }
+        __syncthreads();
+        w = VT;
+    }
+
+    for (; w < run_to; w *= 2) {
+        int cnt = 0;
+        if (p0 < count) {
+            const int a0 = p0 & ~(2 * w - 1);
+            const int d = p0 - a0;
+            const int m = (count - a0) < w ? (count - a0) : w;
+            const int nb_raw = count - a0 - w;
+            const int nb = nb_raw <= 0 ? 0 : (nb_raw < w ? nb_raw : w);
+            const int b0 = a0 + w;
+            cnt = (m + nb - d) < VT ? (m + nb - d) : VT;
+            int a = corank_padded(d, sk, a0, m, b0, nb);
+            int b = d - a;
+            uint32_t ak = (a < m) ? sk[pad32(a0 + a)] : 0u;
+            uint32_t bk = (b < nb) ? sk[pad32(b0 + b)] : 0u;
+#pragma unroll
+            for (int i = 0; i < VT; ++i) {
+                if (i < cnt) {
+                    const bool take_a = (b >= nb) || (a < m && ak <= bk);
+                    if (take_a) {
+                        k[i] = ak;
+                        if (V) v[i] = sv[pad32(a0 + a)];
+                        ++a;
+                        if (a < m) ak = sk[pad32(a0 + a)];
+                    } else {
+                        k[i] = bk;
+                        if (V) v[i] = sv[pad32(b0 + b)];
+                        ++b;
+                        if (b < nb) bk = sk[pad32(b0 + b)];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < VT; ++i) {
+            if (i < cnt) {
+                sk[pad32(p0 + i)] = k[i];
+                if (V) sv[pad32(p0 + i)] = v[i];
+            }
+        }
+        __syncthreads();
+    }
+
+    for (int p = tid; p < count; p += NT) {
+        out_k[base + p] = sk[pad32(p)];
+        if (V) out_v[base + p] = sv[pad32(p)];
+    }
+}
+
+}  // namespace om

@@ -1,0 +1,81 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every
+function include/ordmerge.h declares, and rejects bad arguments on the host
+before touching the device (no compute calls: these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ordmerge.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    path = __graft_entry__._lib_build_module().build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(om_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for required in ["om_corank_i32", "om_merge_i32", "om_merge_pairs_u32", "om_merge_sort_u32"]:
+        assert required in names
+    assert len(names) >= 10
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_status_strings(lib):
+    import ordered_merge_gb300 as om
+
+    for s in range(6):
+        assert om.lib().om_status_string(s).decode().startswith("OM_")
+
+
+def test_host_argument_checks():
+    """Invalid arguments are rejected by host code with a status, not a crash,
+    and never reach the GPU."""
+    import ordered_merge_gb300 as om
+
+    L = om.lib()
+    # negative lengths
+    assert L.om_merge_i32(None, -1, None, 0, None, None) == om.OM_EINVAL
+    assert L.om_merge_pairs_u32(None, None, 0, None, None, -5, None, None, None) == om.OM_EINVAL
+    assert L.om_merge_sort_u32(None, None, -2, None) == om.OM_EINVAL
+    # empty merge / trivial sort are no-ops
+    assert L.om_merge_i32(None, 0, None, 0, None, None) == om.OM_OK
+    assert L.om_merge_sort_u32(None, None, 1, None) == om.OM_OK
+    # NULL with a nonzero length
+    assert L.om_merge_i32(None, 4, 0x1000, 4, 0x2000, None) == om.OM_EINVAL
+    assert L.om_merge_i32(0x1000, 4, 0x2000, 4, None, None) == om.OM_EINVAL
+    # misaligned pointers
+    assert L.om_merge_i32(0x1002, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+    # output overlapping an input
+    assert L.om_merge_i32(0x1000, 4, 0x2000, 4, 0x1008, None) == om.OM_EINVAL
+    assert L.om_merge_i32(0x1000, 4, 0x2000, 4, 0x1FF0, None) == om.OM_EINVAL
+    # m + n overflow
+    assert L.om_merge_i32(0x1000, 2**62, 0x2000, 2**62, 0x3000, None) == om.OM_ERANGE
+    # pairs: key/value 16-byte phase mismatch
+    assert L.om_merge_pairs_u32(0x1000, 0x2004, 4, 0x3000, 0x4000, 4, 0x5000, 0x6000, None) == om.OM_EINVAL
+    # sort: vals overlapping keys
+    assert L.om_merge_sort_u32(0x1000, 0x1008, 16, None) == om.OM_EINVAL
+    # co-rank: k outside [0, m+n], negative length
+    assert L.om_corank_i32(11, 0x1000, 5, 0x2000, 5) == -om.OM_ERANGE
+    assert L.om_corank_i32(-1, 0x1000, 5, 0x2000, 5) == -om.OM_ERANGE
+    assert L.om_corank_i32(0, 0x1000, -5, 0x2000, 5) == -om.OM_EINVAL
+    # co-rank with one side empty is forced and needs no device
+    assert L.om_corank_i32(3, None, 0, 0x2000, 5) == 0
+    assert L.om_corank_i32(3, 0x1000, 5, None, 0) == 3

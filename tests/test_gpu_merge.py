@@ -1,0 +1,140 @@
+"""GPU parity of om_merge_i32 and om_corank_i32 against the CPU oracle:
+element-by-element, bit-exact, with guard bands around every output.
+
+Sizes span one sub-tile, many sub-tiles, many output ranges and ragged
+tails; edge cases cover empty sides, one-element sides, all-equal keys,
+disjoint value ranges in both orders, extreme int32 values and pointers that
+are not 16-byte aligned.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import dev_i32, guarded_empty, guards_intact, host, shifted
+
+pytestmark = pytest.mark.gpu
+
+
+def run_merge(om, A_np, B_np, offs=(0, 0, 0)):
+    A = shifted(dev_i32(A_np), offs[0])
+    B = shifted(dev_i32(B_np), offs[1])
+    total = A_np.size + B_np.size
+    buf, C = guarded_empty(total, offs[2])
+    om.merge_i32(A, B, C)
+    torch.cuda.synchronize()
+    assert om.device_error() == 0
+    assert guards_intact(buf, total, offs[2]), "merge wrote outside C"
+    return host(C)
+
+
+def check(om, A_np, B_np, offs=(0, 0, 0)):
+    got = run_merge(om, A_np, B_np, offs)
+    want = oracle.merge_i32(A_np, B_np)
+    if not np.array_equal(got, want):
+        bad = int(np.flatnonzero(got != want)[0])
+        raise AssertionError(f"first mismatch at {bad}: got {got[bad]}, want {want[bad]} "
+                             f"(m={A_np.size}, n={B_np.size}, offs={offs})")
+
+
+def sorted_rand(rng, size, lo, hi):
+    return np.sort(rng.integers(lo, hi, size, dtype=np.int64)).astype(np.int32)
+
+
+def test_pages_worked_example(gpu):
+    A = np.array([1, 7, 8, 9, 10], dtype=np.int32)
+    B = np.array([7, 10, 10, 12], dtype=np.int32)
+    check(gpu, A, B)
+    dA, dB = dev_i32(A), dev_i32(B)
+    assert [gpu.corank_i32(k, dA, dB) for k in (0, 3, 6, 9)] == [0, 2, 5, 5]
+
+
+def test_tie_case(gpu):
+    check(gpu, np.array([1, 1, 2, 3], np.int32), np.array([1, 2, 2, 4], np.int32))
+
+
+@pytest.mark.parametrize("m,n", [(0, 0), (0, 1), (1, 0), (0, 5000), (5000, 0), (1, 1), (3, 1), (1, 3),
+                                 (1919, 1), (960, 960), (961, 960), (1920, 1920), (7, 100000),
+                                 (100000, 7), (12345, 54321), (250001, 249999)])
+def test_shapes(gpu, m, n):
+    rng = np.random.default_rng(m * 7919 + n)
+    check(gpu, sorted_rand(rng, m, -1000, 1000), sorted_rand(rng, n, -1000, 1000))
+
+
+@pytest.mark.parametrize("span", [1, 2, 16, 1 << 31])
+def test_value_spans(gpu, span):
+    rng = np.random.default_rng(span)
+    lo, hi = (-span, span) if span > 1 else (5, 6)
+    check(gpu, sorted_rand(rng, 300007, lo, hi), sorted_rand(rng, 299993, lo, hi))
+
+
+def test_all_equal_keys(gpu):
+    check(gpu, np.full(100003, 42, np.int32), np.full(77777, 42, np.int32))
+
+
+def test_disjoint_both_orders(gpu):
+    A = np.arange(0, 200000, dtype=np.int32)
+    B = np.arange(200000, 350001, dtype=np.int32)
+    check(gpu, A, B)
+    check(gpu, B, A)
+
+
+def test_int32_extremes(gpu):
+    lo, hi = np.iinfo(np.int32).min, np.iinfo(np.int32).max
+    A = np.array([lo, lo, -1, 0, hi, hi], np.int32)
+    B = np.array([lo, 0, 0, 1, hi], np.int32)
+    check(gpu, A, B)
+    rng = np.random.default_rng(4)
+    A = np.sort(np.concatenate([np.full(5000, lo), rng.integers(lo, hi, 5000), np.full(5000, hi)])).astype(np.int32)
+    B = np.sort(np.concatenate([np.full(3000, hi), np.full(3000, lo)])).astype(np.int32)
+    check(gpu, A, B)
+
+
+@pytest.mark.parametrize("offs", [(1, 0, 0), (0, 3, 0), (0, 0, 2), (1, 2, 3), (3, 3, 1)])
+def test_misaligned_pointers(gpu, offs):
+    rng = np.random.default_rng(sum(offs))
+    check(gpu, sorted_rand(rng, 54321, -500, 500), sorted_rand(rng, 43210, -500, 500), offs)
+    check(gpu, sorted_rand(rng, 13, -5, 5), sorted_rand(rng, 1, -5, 5), offs)
+
+
+@pytest.mark.parametrize("workload", ["evens_odds", "skewed", "uniform"])
+def test_workloads_scaled(gpu, workload):
+    d = synth.make_host(workload, scale_log2=6)
+    check(gpu, d["A"], d["B"])
+
+
+def test_evens_odds_full_size(gpu):
+    d = synth.make_host("evens_odds")
+    check(gpu, d["A"], d["B"])
+
+
+def test_corank_against_oracle(gpu):
+    rng = np.random.default_rng(8)
+    for span in [3, 1 << 20, 1 << 31]:
+        A = sorted_rand(rng, 70001, -span, span)
+        B = sorted_rand(rng, 50003, -span, span)
+        dA, dB = dev_i32(A), dev_i32(B)
+        ks = np.concatenate([[0, 1, A.size, B.size, A.size + B.size - 1, A.size + B.size],
+                             rng.integers(0, A.size + B.size + 1, 200)]).astype(np.int64)
+        got = host(gpu.corank_i32_batch(torch.from_numpy(ks).cuda(), dA, dB))
+        want = np.array([oracle.corank_pages(int(k), A, B) for k in ks])
+        assert np.array_equal(got, want)
+        for k in ks[:20]:
+            assert gpu.corank_i32(int(k), dA, dB) == oracle.corank_count(int(k), A, B)
+
+
+def test_merge_on_side_stream(gpu):
+    rng = np.random.default_rng(12)
+    A, B = sorted_rand(rng, 100000, 0, 1000), sorted_rand(rng, 90000, 0, 1000)
+    s = torch.cuda.Stream()
+    dA, dB = dev_i32(A), dev_i32(B)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        C = gpu.merge_i32(dA, dB)
+    s.synchronize()
+    assert np.array_equal(host(C), oracle.merge_i32(A, B))
+
+
+def test_device_error_word_clear(gpu):
+    assert gpu.device_error() == 0
