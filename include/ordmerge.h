@@ -133,6 +133,36 @@ om_status om_trace_read(int kind, int64_t *launches, double *total_ms);
 /* Number of kernels this library has launched since load. */
 uint64_t om_launch_count(void);
 
+/* ---- merge without allocating ------------------------------------------ */
+
+/*
+ * The pages have no counterpart to this call: it is a library convenience.
+ *
+ * Same result and kernels as om_merge_i32, but it allocates nothing: the
+ * co-rank splitters go to a fixed 64 KiB array that the library keeps in
+ * device memory (a file-scope __device__ object, held on every GPU that loads
+ * the library until the process exits).  For callers that cannot allocate
+ * device memory on the call path: processes whose device memory is reserved
+ * in full by another allocator, so that a stream-ordered allocation could
+ * fail, and code with latency bounds that must not enter an allocator.
+ *
+ *  - m + n may be at most 1,006,510,080 (8191 ranges of 64 sub-tiles of 1920
+ *    outputs); larger merges return OM_ERANGE and launch nothing.
+ *  - The first call on each device does a one-time set-up there (it looks up
+ *    the array's device address and sets kernel attributes); make that first
+ *    call before any stream capture.
+ *  - All calls on a device share the array.  Each call's kernels write every
+ *    slot they read before reading it, so nothing needs clearing, but calls
+ *    whose kernels overlap on the GPU (e.g. on different streams) race on
+ *    the array and can produce wrong output: order them on one stream or
+ *    with events.
+ *  - With tracing off (the default) no call of this function allocates
+ *    anything, on the device or the host; argument rules and errors are those
+ *    of om_merge_i32.
+ */
+om_status om_merge_i32_noalloc(const int32_t *A, int64_t m, const int32_t *B,
+                               int64_t n, int32_t *C, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -435,4 +435,78 @@ om_status om_trace_read(int kind, int64_t* launches, double* total_ms) {
 
 uint64_t om_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+// ------------------------------------------------- merge without allocating --
+//
+// om_merge_i32_noalloc: the same partition + tile-merge kernels as
+// om_merge_i32, but the splitter scratch lives in the fixed array below
+// instead of coming from cudaMallocAsync.  It exists for callers that must
+// not allocate device memory on the call path: a process whose device memory
+// is already reserved in full by another allocator (a framework's caching
+// allocator, a fixed arena), where a stream-ordered allocation could fail for
+// lack of memory that is in fact idle; and code with hard latency bounds that
+// must not enter an allocator (pool growth, allocator locks) per call.
+//
+// The array is a file-scope __device__ object: every GPU that loads this
+// library holds its 64 KiB until the process exits, and all calls on a device
+// share it.  The splitters a call needs are all written by its own partition
+// kernel before its tile-merge kernel reads them, so nothing has to be
+// cleared between calls; but two calls whose kernels overlap on the GPU (for
+// example on two streams) race on the array and may produce wrong output.
+constexpr int64_t kNoAllocSplits = 8192;  // int64 slots: 64 KiB
+constexpr int64_t kNoAllocMaxSubtilesPerRange = 64;
+constexpr int64_t kNoAllocMaxOutputs = (kNoAllocSplits - 1) * kNoAllocMaxSubtilesPerRange * MergeCfg::T;
+
+static __device__ __align__(256) int64_t g_noalloc_splits[kNoAllocSplits];
+
+static std::mutex g_noalloc_mu;
+static int64_t* g_noalloc_addr[128];  // device address of g_noalloc_splits, per device
+
+// Once per device, with that device current: the device address of the
+// array.  (In host code the array's name is only a host-side stand-in.)
+static om_status noalloc_scratch(int64_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return OM_ECUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        int64_t* ptr = nullptr;
+        if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_splits) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return OM_ECUDA;
+        }
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return OM_OK;
+}
+
+om_status om_merge_i32_noalloc(const int32_t* A, int64_t m, const int32_t* B, int64_t n, int32_t* C,
+                               void* stream) {
+    if (m < 0 || n < 0) return OM_EINVAL;
+    if (m > INT64_MAX - n) return OM_ERANGE;
+    const int64_t total = m + n;
+    if (total == 0) return OM_OK;
+    if (total > kNoAllocMaxOutputs) return OM_ERANGE;  // beyond the fixed splitter array
+    if ((m > 0 && A == nullptr) || (n > 0 && B == nullptr) || C == nullptr) return OM_EINVAL;
+    if (misaligned4(A) || misaligned4(B) || misaligned4(C)) return OM_EINVAL;
+    if (overlaps(C, total, A, m) || overlaps(C, total, B, n)) return OM_EINVAL;
+
+    DeviceState* d = nullptr;
+    om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    int64_t* split = nullptr;
+    s = noalloc_scratch(&split);
+    if (s != OM_OK) return s;
+
+    const int64_t subtiles = (total + MergeCfg::T - 1) / MergeCfg::T;
+    int64_t per_range = subtiles_per_range(subtiles, d->sm_count);
+    const int64_t fit = (subtiles + kNoAllocSplits - 2) / (kNoAllocSplits - 1);  // ranges must fit the array
+    if (per_range < fit) per_range = fit;
+    const int64_t range_len = per_range * MergeCfg::T;
+    const int64_t nranges = (total + range_len - 1) / range_len;
+    if (nranges + 1 > kNoAllocSplits) return OM_ERANGE;
+    MergeGeom<int32_t> g{A, nullptr, B, nullptr, C, nullptr, m, n, 0, range_len, nranges, nranges};
+    const cudaError_t e = launch_merge<int32_t, false>(g, split, d, (cudaStream_t)stream);
+    return e == cudaSuccess ? OM_OK : cuda_fail(e);
+}
+
 }  // extern "C"
