@@ -237,7 +237,7 @@ def bench_ours(args):
     dist_init(world, "nccl")
 
     wl = args.workload
-    d = synth.make_device(wl, device)
+    d = synth.make_device(wl, device, scale_log2=args.scale_log2)
     stream = torch.cuda.current_stream(device)
 
     if wl in ("uniform", "evens_odds", "skewed"):
@@ -425,6 +425,7 @@ def bench_ours(args):
             "config": {
                 "workload": WORKLOADS[wl],
                 "name": wl,
+                "scale_log2": args.scale_log2,
                 "m": m,
                 "n": n,
                 "l2": "inputs larger than L2 (no flush)" if total * 4 > 2 * 129e6 else
@@ -516,6 +517,8 @@ def main(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--scale-log2", type=int, default=0,
+                   help="shrink the workload by 2^-s (profiling small cases; 0 = the named size)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")

@@ -36,6 +36,8 @@ static __device__ int64_t g_corank_slot;
 struct DeviceState {
     bool ready = false;
     int sm_count = 0;
+    int resident_merge = 0;  // tile-merge CTAs resident per SM (keys only / with values)
+    int resident_merge_v = 0;
     uint32_t* err = nullptr;
     int64_t* corank_slot = nullptr;
 };
@@ -72,6 +74,15 @@ static om_status device_state(DeviceState** out) {
         e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, true>, block_sort_smem_bytes<SmallMergeCfg, true>());
         e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, false>, block_sort_smem_bytes<SmallMergeCfg, false>());
         if (e != cudaSuccess) return OM_ECUDA;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge,
+                                                          tile_merge_kernel<MergeCfg, int32_t, false>, MergeCfg::NT,
+                                                          TileSmem<MergeCfg, false>::total);
+        e = e ? e : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge_v,
+                                                                   tile_merge_kernel<MergeCfg, uint32_t, true>,
+                                                                   MergeCfg::NT, TileSmem<MergeCfg, true>::total);
+        if (e != cudaSuccess) return OM_ECUDA;
+        if (d.resident_merge < 1) d.resident_merge = 1;
+        if (d.resident_merge_v < 1) d.resident_merge_v = 1;
         d.ready = true;
     }
     *out = &d;
@@ -161,13 +172,16 @@ static int64_t env_int(const char* name, int64_t fallback) {
     return (end != s && v > 0) ? (int64_t)v : fallback;
 }
 
-// Sub-tiles per CTA output range: long ranges amortise each CTA's start-up
-// (the first chunks' latency), but there must be enough ranges to fill every
-// SM several times over.  OM_SUBTILES_PER_RANGE overrides (tuning).
-static int64_t subtiles_per_range(int64_t subtiles, int sm_count) {
-    int64_t s = subtiles / ((int64_t)sm_count * 32);
+// Sub-tiles per CTA output range.  Every range has the same number of
+// outputs, so the merge costs the same in each; the grid is sized to a whole
+// number of waves of resident CTAs (OM_WAVES, default 1) so that no SM idles
+// through a partial last wave.  Long ranges also amortise each CTA's start-up
+// (the latency of its first chunks).  OM_SUBTILES_PER_RANGE overrides.
+static int64_t subtiles_per_range(int64_t subtiles, int64_t resident_ctas) {
+    const int64_t waves = env_int("OM_WAVES", 1);
+    const int64_t slots = resident_ctas * waves;
+    int64_t s = (subtiles + slots - 1) / slots;
     if (s < 1) s = 1;
-    if (s > 64) s = 64;
     return env_int("OM_SUBTILES_PER_RANGE", s);
 }
 
@@ -196,7 +210,8 @@ static om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K*
     if (s != OM_OK) return s;
     const int64_t total = m + n;
     const int64_t subtiles = (total + MergeCfg::T - 1) / MergeCfg::T;
-    const int64_t range_len = subtiles_per_range(subtiles, d->sm_count) * MergeCfg::T;
+    const int64_t resident = (int64_t)d->sm_count * (V ? d->resident_merge_v : d->resident_merge);
+    const int64_t range_len = subtiles_per_range(subtiles, resident) * MergeCfg::T;
     const int64_t nranges = (total + range_len - 1) / range_len;
     if (nranges > 0x7fffffff) return OM_ERANGE;
     MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
@@ -222,7 +237,8 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
     int passes = 0;
     for (int64_t r = kRunLen; r < n; r *= 2) ++passes;
     const int64_t subtiles = (n + MergeCfg::T - 1) / MergeCfg::T;
-    const int64_t range_len = subtiles_per_range(subtiles, d->sm_count) * MergeCfg::T;
+    const int64_t resident = (int64_t)d->sm_count * (V ? d->resident_merge_v : d->resident_merge);
+    const int64_t range_len = subtiles_per_range(subtiles, resident) * MergeCfg::T;
     // splitter slots for the largest late pass: ranges of every pair, plus one
     const int64_t max_ranges = (n + range_len - 1) / range_len + (n + 2 * kRunLen - 1) / (2 * kRunLen) + 1;
 
@@ -498,7 +514,7 @@ om_status om_merge_i32_noalloc(const int32_t* A, int64_t m, const int32_t* B, in
     if (s != OM_OK) return s;
 
     const int64_t subtiles = (total + MergeCfg::T - 1) / MergeCfg::T;
-    int64_t per_range = subtiles_per_range(subtiles, d->sm_count);
+    int64_t per_range = subtiles_per_range(subtiles, (int64_t)d->sm_count * d->resident_merge);
     const int64_t fit = (subtiles + kNoAllocSplits - 2) / (kNoAllocSplits - 1);  // ranges must fit the array
     if (per_range < fit) per_range = fit;
     const int64_t range_len = per_range * MergeCfg::T;

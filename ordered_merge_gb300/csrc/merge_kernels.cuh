@@ -171,32 +171,40 @@ struct TileCfg {
     static constexpr int NCH_LOG2 = RING_LOG2 - CH_LOG2;
     static constexpr int NCH = 1 << NCH_LOG2;
     static constexpr int STAGE = T + 8;
+    // largest power of two <= T: the first step of the fixed-step search
+    static constexpr int SEARCH_TOP = (T >= 4096) ? 4096 : (T >= 2048) ? 2048 : (T >= 1024) ? 1024
+                                    : (T >= 512) ? 512 : (T >= 256) ? 256 : 128;
     static_assert(VT % 2 == 1, "odd VT keeps the register->stage writes free of bank conflicts");
     static_assert(T % 4 == 0, "sub-tile boundaries stay 16-byte aligned in C");
     static_assert(T + CH <= RING, "a window of T plus one chunk must fit in the ring");
     static_assert(CH >= 4 && NCH >= 2, "chunks are whole 16-byte groups");
+    static_assert(2 * SEARCH_TOP > T, "the fixed-step search must reach every co-rank");
 };
 
+// Shared memory: keys of both rings back to back (A ring, then B ring, so one
+// masked index addresses either), values likewise, the output stage, the
+// chunk barriers of both sides, the stage barrier and two broadcast words.
 template <typename Cfg, bool V>
 struct TileSmem {
-    static constexpr size_t ring_bytes = (size_t)Cfg::RING * 4 * (V ? 4 : 2);
+    static constexpr size_t ring_bytes = (size_t)2 * Cfg::RING * 4 * (V ? 2 : 1);
     static constexpr size_t stage_bytes = (size_t)Cfg::STAGE * 4 * (V ? 2 : 1);
-    static constexpr size_t bar_bytes = (size_t)2 * Cfg::NCH * 8;
+    static constexpr size_t bar_bytes = (size_t)(2 * Cfg::NCH + 1) * 8;
     static constexpr size_t total = ring_bytes + stage_bytes + bar_bytes + 16;
 };
 
 // Streaming state of one input side (A or B) of one CTA's output range.
 // Positions are in "u" units: u = element index + (address / 4) mod 4 of
-// the segment's first element, so u % 4 == 0 exactly at 16-byte boundaries.
+// the side's first element, so u % 4 == 0 exactly at 16-byte boundaries.
 struct SideStream {
-    const char* base16;   // 16-byte aligned address of u = 0 (keys)
-    const char* vbase16;  // same for values
-    int64_t arr_lo, arr_hi;  // u extent of the whole side array
-    int64_t u_lo, u_hi;      // u extent of this CTA's part
-    int64_t head;            // next unconsumed u (A_consumed / B_consumed)
-    int64_t c_first, c_last; // chunk indices covering [u_lo, u_hi)
-    int64_t next_issue;      // next chunk to request (thread 0)
-    int64_t next_wait;       // next chunk this thread has not yet waited for
+    const char* base16;       // 16-byte aligned address of u = 0 (keys)
+    const char* vbase16;      // same for values
+    int64_t arr_lo, arr_hi;   // u extent of the whole side array
+    int64_t arr_lo4, arr_hi4; // its 16-byte-aligned interior
+    int64_t u_lo, u_hi;       // u extent of this CTA's part
+    int64_t head;             // next unconsumed u (A_consumed / B_consumed)
+    int64_t c_first, c_last;  // chunk indices covering [u_lo, u_hi)
+    int64_t next_issue;       // next chunk to request (thread 0)
+    int next_wait;            // next chunk (relative to c_first) not yet waited for
 };
 
 template <typename Cfg>
@@ -208,46 +216,62 @@ __device__ __forceinline__ void side_init(SideStream& s, const void* keys, const
     s.vbase16 = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(vals) & ~uintptr_t(15));
     s.arr_lo = mis;
     s.arr_hi = mis + len;
+    s.arr_lo4 = (s.arr_lo + 3) & ~int64_t(3);
+    s.arr_hi4 = s.arr_hi & ~int64_t(3);
     s.u_lo = mis + lo;
     s.u_hi = mis + hi;
     s.head = s.u_lo;
     s.c_first = s.u_lo >> Cfg::CH_LOG2;
     s.c_last = (s.u_hi > s.u_lo) ? ((s.u_hi - 1) >> Cfg::CH_LOG2) : s.c_first - 1;
     s.next_issue = s.c_first;
-    s.next_wait = s.c_first;
+    s.next_wait = 0;
 }
 
-// Thread 0 only: request chunk c of side s into its ring slots.  The 16-byte
-// aligned body goes through one bulk copy per array; the at most 3 + 3
-// elements at the two ends of the side array that do not fill a 16-byte group
-// are loaded with plain loads.
+// Thread 0 only: request chunk c of side s into its ring slots.  A chunk
+// that lies wholly inside the CTA's part and the array's aligned interior is
+// one bulk copy per array.  Otherwise the 16-byte aligned body goes through
+// a bulk copy and the at most 3 + 3 elements at the two ends of the side
+// array that do not fill a 16-byte group are loaded with plain loads; those
+// stores are published to the other threads by the barrier's arrive
+// (release) and their wait (acquire).
 template <typename Cfg, typename K, bool V>
 __device__ __forceinline__ void issue_chunk(SideStream& s, int64_t c, K* ring_k, uint32_t* ring_v,
                                             uint64_t* bars, uint64_t policy) {
-    const int64_t s0 = (c << Cfg::CH_LOG2) > s.u_lo ? (c << Cfg::CH_LOG2) : s.u_lo;
-    const int64_t e0 = ((c + 1) << Cfg::CH_LOG2) < s.u_hi ? ((c + 1) << Cfg::CH_LOG2) : s.u_hi;
-    const int64_t arr_lo4 = (s.arr_lo + 3) & ~int64_t(3);
-    const int64_t arr_hi4 = s.arr_hi & ~int64_t(3);
+    const int64_t cs = c << Cfg::CH_LOG2;
+    const int64_t ce = cs + Cfg::CH;
+    uint64_t* bar = &bars[(int)(c - s.c_first) & (Cfg::NCH - 1)];
+    if (cs >= s.u_lo && ce <= s.u_hi && cs >= s.arr_lo4 && ce <= s.arr_hi4) {
+        const uint32_t slot = (uint32_t)cs & Cfg::RMASK;
+        mbar_arrive_expect_tx(bar, (uint32_t)Cfg::CH * 4u * (V ? 2u : 1u));
+        bulk_copy_g2s(ring_k + slot, s.base16 + 4 * cs, Cfg::CH * 4, bar, policy);
+        if (V) bulk_copy_g2s(ring_v + slot, s.vbase16 + 4 * cs, Cfg::CH * 4, bar, policy);
+        return;
+    }
+    const int64_t s0 = cs > s.u_lo ? cs : s.u_lo;
+    const int64_t e0 = ce < s.u_hi ? ce : s.u_hi;
     int64_t bs = s0 & ~int64_t(3);
-    if (bs < arr_lo4) bs = arr_lo4;
+    if (bs < s.arr_lo4) bs = s.arr_lo4;
     int64_t be = (e0 + 3) & ~int64_t(3);
-    if (be > arr_hi4) be = arr_hi4;
-    uint64_t* bar = &bars[(c - s.c_first) & (Cfg::NCH - 1)];
+    if (be > s.arr_hi4) be = s.arr_hi4;
     const K* gk = reinterpret_cast<const K*>(s.base16);
     const uint32_t* gv = reinterpret_cast<const uint32_t*>(s.vbase16);
     bool plain = false;
-    auto load_plain = [&](int64_t u) {
+    uint32_t bytes = 0;
+    int64_t p0 = s0, p1 = e0, q0 = e0, q1 = e0;  // plain-load intervals [p0,p1) and [q0,q1)
+    if (be > bs) {
+        p1 = bs;
+        q0 = be;
+        bytes = (uint32_t)(be - bs) * 4u;
+    }
+    for (int64_t u = p0; u < p1; ++u) {
         ring_k[(uint32_t)u & Cfg::RMASK] = gk[u];
         if (V) ring_v[(uint32_t)u & Cfg::RMASK] = gv[u];
         plain = true;
-    };
-    uint32_t bytes = 0;
-    if (be > bs) {
-        for (int64_t u = s0; u < bs; ++u) load_plain(u);
-        for (int64_t u = be; u < e0; ++u) load_plain(u);
-        bytes = (uint32_t)(be - bs) * 4u;
-    } else {
-        for (int64_t u = s0; u < e0; ++u) load_plain(u);
+    }
+    for (int64_t u = q0; u < q1; ++u) {
+        ring_k[(uint32_t)u & Cfg::RMASK] = gk[u];
+        if (V) ring_v[(uint32_t)u & Cfg::RMASK] = gv[u];
+        plain = true;
     }
     if (plain) fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar, V ? 2 * bytes : bytes);
@@ -272,63 +296,105 @@ __device__ __forceinline__ void refill(SideStream& s, K* ring_k, uint32_t* ring_
 
 // Every thread: wait until all chunks covering u < need_end have landed.
 template <typename Cfg>
-__device__ __forceinline__ bool wait_window(SideStream& s, int64_t need_end, uint64_t* bars,
-                                            uint32_t* err) {
+__device__ __forceinline__ bool wait_window(SideStream& s, int64_t need_end, uint64_t* bars, uint32_t* err) {
     if (need_end <= s.head) return true;
-    const int64_t c_need = (need_end - 1) >> Cfg::CH_LOG2;
-    for (; s.next_wait <= c_need; ++s.next_wait) {
-        const int64_t rel = s.next_wait - s.c_first;
-        if (!mbar_wait_bounded(&bars[rel & (Cfg::NCH - 1)], (uint32_t)(rel >> Cfg::NCH_LOG2) & 1u, err))
+    const int need = (int)(((need_end - 1) >> Cfg::CH_LOG2) - s.c_first);
+    for (; s.next_wait <= need; ++s.next_wait) {
+        if (!mbar_wait_bounded(&bars[s.next_wait & (Cfg::NCH - 1)], (uint32_t)(s.next_wait >> Cfg::NCH_LOG2) & 1u,
+                               err))
             return false;
     }
     return true;
 }
 
-// co_rank(d) of two ring windows: A window = ring_a[(ha + x) & mask] for
-// x < wa, B window likewise.  Same bounded bisection as corank_global.
+// co_rank(d) of the two ring windows, A = ring[(ha + x) & mask] and
+// B = ring[RING | ((hb + x) & mask)]: the largest i in [lo, hi] with i == lo
+// or A[i-1] <= B[d-i], by a fixed sequence of power-of-two steps (no data
+// dependent trip count, so a warp never diverges on it).
 template <typename Cfg, typename K>
-__device__ __forceinline__ int corank_ring(int d, const K* ra, uint32_t ha, int wa, const K* rb,
-                                           uint32_t hb, int wb) {
-    int lo = d - wb > 0 ? d - wb : 0;
-    int hi = d < wa ? d : wa;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        const K x = ra[(ha + (uint32_t)(mid - 1)) & Cfg::RMASK];
-        const K y = rb[(hb + (uint32_t)(d - mid)) & Cfg::RMASK];
-        if (x <= y) {
-            lo = mid;
-        } else {
-            hi = mid - 1;
+__device__ __forceinline__ int corank_ring(int d, int lo, int hi, const K* ring, uint32_t ha, uint32_t hb) {
+#pragma unroll
+    for (int step = Cfg::SEARCH_TOP; step > 0; step >>= 1) {
+        const int cand = lo + step;
+        if (cand <= hi) {
+            const K x = ring[(ha + (uint32_t)(cand - 1)) & Cfg::RMASK];
+            const K y = ring[Cfg::RING | ((hb + (uint32_t)(d - cand)) & Cfg::RMASK)];
+            if (x <= y) lo = cand;
         }
     }
     return lo;
+}
+
+// Serial merge of VT outputs from the split (a, b) of the two windows, with
+// selects instead of branches: take A unless B's head is strictly smaller
+// (ties go to A).  GUARD adds the exhaustion tests needed when a window ends
+// before the sub-tile does (the last sub-tile of a range); without GUARD all
+// VT steps run.  Returns the A position after the last step.
+template <typename Cfg, typename K, bool V, bool GUARD>
+__device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, int wb, const K* ring,
+                                                 const uint32_t* vring, uint32_t ha, uint32_t hb, K (&keys)[Cfg::VT],
+                                                 uint32_t (&vals)[Cfg::VT]) {
+    constexpr uint32_t M = Cfg::RMASK;
+    uint32_t ai = ha + (uint32_t)a;
+    uint32_t bi = hb + (uint32_t)b;
+    const uint32_t a_end = ha + (uint32_t)wa;
+    const uint32_t b_end = hb + (uint32_t)wb;
+    const uint32_t ia = ai & M, ib = Cfg::RING | (bi & M);
+    K ak = ring[ia];
+    K bk = ring[ib];
+    uint32_t av = 0, bv = 0;
+    if (V) {
+        av = vring[ia];
+        bv = vring[ib];
+    }
+#pragma unroll
+    for (int v = 0; v < Cfg::VT; ++v) {
+        if (!GUARD || v < cnt) {
+            const bool p = GUARD ? ((bi >= b_end) || ((ai < a_end) && (ak <= bk))) : (ak <= bk);
+            keys[v] = p ? ak : bk;
+            if (V) vals[v] = p ? av : bv;
+            ai += p ? 1u : 0u;
+            bi += p ? 0u : 1u;
+            if (v + 1 < Cfg::VT) {
+                const uint32_t idx = p ? (ai & M) : (Cfg::RING | (bi & M));
+                const K nk = ring[idx];
+                ak = p ? nk : ak;
+                bk = p ? bk : nk;
+                if (V) {
+                    const uint32_t nv = vring[idx];
+                    av = p ? nv : av;
+                    bv = p ? bv : nv;
+                }
+            }
+        }
+    }
+    return ai - ha;
 }
 
 // The tile-merge kernel.  CTA r merges output range r of the geometry:
 // C[k0, k1) from A[i0, i1) and B[j0, j1), where i0 / i1 come from the
 // partition kernel.  It walks the range in sub-tiles of T outputs:
 //   wait for the window chunks -> per-thread co-rank in the ring -> serial
-//   merge of VT outputs -> stage -> barrier -> advance A/B heads by the
-//   sub-tile's co-rank, request freed chunks -> 128-bit stores of the stage.
+//   merge of VT outputs into registers -> stage -> one barrier -> advance the
+//   A/B heads by the sub-tile's co-rank and request the freed chunks ->
+//   bulk store of the stage to C (thread 0, asynchronous).
 template <typename Cfg, typename K, bool V>
 __global__ void __launch_bounds__(Cfg::NT) tile_merge_kernel(MergeGeom<K> g, const int64_t* __restrict__ split,
                                                              uint32_t* err) {
     constexpr int NT = Cfg::NT;
     constexpr int VT = Cfg::VT;
     constexpr int T = Cfg::T;
-    constexpr uint32_t RMASK = Cfg::RMASK;
     using Smem = TileSmem<Cfg, V>;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    K* ring_a = reinterpret_cast<K*>(smem);
-    K* ring_b = ring_a + Cfg::RING;
-    uint32_t* ring_av = V ? reinterpret_cast<uint32_t*>(ring_b + Cfg::RING) : nullptr;
-    uint32_t* ring_bv = V ? ring_av + Cfg::RING : nullptr;
+    K* ring = reinterpret_cast<K*>(smem);                       // [A ring | B ring]
+    uint32_t* vring = V ? reinterpret_cast<uint32_t*>(ring + 2 * Cfg::RING) : nullptr;
     K* stage_k = reinterpret_cast<K*>(smem + Smem::ring_bytes);
     uint32_t* stage_v = V ? reinterpret_cast<uint32_t*>(stage_k + Cfg::STAGE) : nullptr;
     uint64_t* bars_a = reinterpret_cast<uint64_t*>(smem + Smem::ring_bytes + Smem::stage_bytes);
     uint64_t* bars_b = bars_a + Cfg::NCH;
-    int* s_misc = reinterpret_cast<int*>(bars_b + Cfg::NCH);  // [0] a_used, [1] abort
+    uint64_t* bar_stage = bars_b + Cfg::NCH;
+    int* s_misc = reinterpret_cast<int*>(bar_stage + 1);  // [0], [1] a_used by parity; [2] abort
 
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
@@ -352,9 +418,8 @@ __global__ void __launch_bounds__(Cfg::NT) tile_merge_kernel(MergeGeom<K> g, con
     side_init<Cfg>(B, s.bk, s.bv, s.n, j0, j1);
     const uintptr_t caddr = reinterpret_cast<uintptr_t>(s.ck);
     const int64_t misc = (int64_t)((caddr >> 2) & 3);
-    K* cbase16 = reinterpret_cast<K*>(caddr & ~uintptr_t(15));
-    uint32_t* cvbase16 = V ? reinterpret_cast<uint32_t*>(reinterpret_cast<uintptr_t>(s.cv) & ~uintptr_t(15))
-                           : nullptr;
+    char* cbase16 = reinterpret_cast<char*>(caddr & ~uintptr_t(15));
+    char* cvbase16 = V ? reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(s.cv) & ~uintptr_t(15)) : nullptr;
 
     uint64_t policy = 0;
     if (tid == 0) {
@@ -362,113 +427,125 @@ __global__ void __launch_bounds__(Cfg::NT) tile_merge_kernel(MergeGeom<K> g, con
             mbar_init(&bars_a[c], 1);
             mbar_init(&bars_b[c], 1);
         }
+        mbar_init(bar_stage, 1);
         fence_barrier_init();
-        s_misc[1] = 0;
+        s_misc[2] = 0;
         policy = l2_policy_evict_first();
     }
     __syncthreads();
     if (tid == 0) {
-        refill<Cfg, K, V>(A, ring_a, ring_av, bars_a, policy);
-        refill<Cfg, K, V>(B, ring_b, ring_bv, bars_b, policy);
+        refill<Cfg, K, V>(A, ring, vring, bars_a, policy);
+        refill<Cfg, K, V>(B, ring + Cfg::RING, V ? vring + Cfg::RING : nullptr, bars_b, policy);
     }
-    __syncthreads();  // publishes plain-loaded ragged elements
 
     bool aborted = false;
-    for (int64_t kdone = k0; kdone < k1;) {
+    int iter = 0;
+    for (int64_t kdone = k0; kdone < k1; ++iter) {
         const int teff = (int)((k1 - kdone) < T ? (k1 - kdone) : T);
         const int wa = (int)((A.u_hi - A.head) < T ? (A.u_hi - A.head) : T);
         const int wb = (int)((B.u_hi - B.head) < T ? (B.u_hi - B.head) : T);
         bool ok = wait_window<Cfg>(A, A.head + wa, bars_a, err);
         ok = wait_window<Cfg>(B, B.head + wb, bars_b, err) && ok;
-        if (!ok) s_misc[1] = 1;
+        if (!ok) s_misc[2] = 1;
 
-        const uint32_t ha = (uint32_t)A.head & RMASK;
-        const uint32_t hb = (uint32_t)B.head & RMASK;
+        const uint32_t ha = (uint32_t)A.head & Cfg::RMASK;
+        const uint32_t hb = (uint32_t)B.head & Cfg::RMASK;
         const int d = (tid * VT < teff) ? tid * VT : teff;
-        const int cnt = (teff - d < VT) ? teff - d : VT;
-        int a = corank_ring<Cfg, K>(d, ring_a, ha, wa, ring_b, hb, wb);
-        int b = d - a;
-
-        // Serial merge of cnt outputs: take A unless A is exhausted or B's
-        // head is strictly smaller (ties go to A).
         K keys[VT];
         uint32_t vals[VT];
-        K ak = (a < wa) ? ring_a[(ha + a) & RMASK] : K(0);
-        K bk = (b < wb) ? ring_b[(hb + b) & RMASK] : K(0);
-#pragma unroll
-        for (int v = 0; v < VT; ++v) {
-            if (v < cnt) {
-                const bool take_a = (b >= wb) || (a < wa && ak <= bk);
-                if (take_a) {
-                    keys[v] = ak;
-                    if (V) vals[v] = ring_av[(ha + a) & RMASK];
-                    ++a;
-                    if (a < wa) ak = ring_a[(ha + a) & RMASK];
-                } else {
-                    keys[v] = bk;
-                    if (V) vals[v] = ring_bv[(hb + b) & RMASK];
-                    ++b;
-                    if (b < wb) bk = ring_b[(hb + b) & RMASK];
-                }
-            }
+        const bool full = (teff == T) && (wa == T) && (wb == T);  // uniform across the CTA
+        int cnt = VT;
+        uint32_t apos;
+        if (full) {
+            const int a = corank_ring<Cfg, K>(d, 0, d, ring, ha, hb);
+            apos = merge_serial<Cfg, K, V, false>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
+        } else {
+            cnt = (teff - d < VT) ? teff - d : VT;
+            const int lo = d - wb > 0 ? d - wb : 0;
+            const int hi = d < wa ? d : wa;
+            const int a = corank_ring<Cfg, K>(d, lo, hi, ring, ha, hb);
+            apos = merge_serial<Cfg, K, V, true>(a, d - a, cnt, wa, wb, ring, vring, ha, hb, keys, vals);
         }
-        if (tid == NT - 1) s_misc[0] = a;  // = co_rank(teff): the A elements this sub-tile used
+        if (tid == NT - 1) s_misc[iter & 1] = (int)apos;  // = co_rank(teff): A elements this sub-tile used
 
-        const int off = (int)((misc + kdone) & 3);
+        // The stage is free once the bulk store of the previous sub-tile has
+        // read it: thread 0 waits for that and arrives on the stage barrier.
+        if (iter > 0) {
+            if (tid == 0) {
+                bulk_wait_read_all();
+                mbar_arrive(bar_stage);
+            }
+            if (!mbar_wait_bounded(bar_stage, (uint32_t)(iter - 1) & 1u, err)) s_misc[2] = 1;
+        }
+        const int off = (int)misc;  // stage slot of output k is k - kdone + (misc + kdone) % 4
+        if (full) {
 #pragma unroll
-        for (int v = 0; v < VT; ++v) {
-            if (v < cnt) {
+            for (int v = 0; v < VT; ++v) {
                 stage_k[off + d + v] = keys[v];
                 if (V) stage_v[off + d + v] = vals[v];
             }
-        }
-        __syncthreads();  // ring reads done, stage written, a_used published
-        if (s_misc[1]) {
-            aborted = true;
-            break;
-        }
-        const int a_used = s_misc[0];
-        A.head += a_used;
-        B.head += teff - a_used;
-        if (tid == 0) {
-            refill<Cfg, K, V>(A, ring_a, ring_av, bars_a, policy);
-            refill<Cfg, K, V>(B, ring_b, ring_bv, bars_b, policy);
-        }
-
-        // C[kdone, kdone + teff) <- stage; u = misc + k, stage slot = u - g0.
-        const int64_t cu0 = misc + kdone;
-        const int64_t g0 = cu0 & ~int64_t(3);
-        const int ngroups = (int)((((cu0 + teff + 3) & ~int64_t(3)) - g0) >> 2);
-        for (int q = tid; q < ngroups; q += NT) {
-            const int64_t gu = g0 + 4 * q;
-            if (gu >= cu0 && gu + 4 <= cu0 + teff) {
-                st_global_cs_v4(cbase16 + gu, *reinterpret_cast<const uint4*>(stage_k + 4 * q));
-                if (V) st_global_cs_v4(cvbase16 + gu, *reinterpret_cast<const uint4*>(stage_v + 4 * q));
-            } else {
-                for (int e = 0; e < 4; ++e) {
-                    const int64_t u = gu + e;
-                    if (u >= cu0 && u < cu0 + teff) {
-                        cbase16[u] = stage_k[4 * q + e];
-                        if (V) cvbase16[u] = stage_v[4 * q + e];
-                    }
+        } else {
+#pragma unroll
+            for (int v = 0; v < VT; ++v) {
+                if (v < cnt) {
+                    stage_k[off + d + v] = keys[v];
+                    if (V) stage_v[off + d + v] = vals[v];
                 }
             }
         }
+        fence_proxy_async_smem();  // stage writes -> visible to the bulk store
+        __syncthreads();           // ring reads done, stage written, a_used published
+        if (s_misc[2]) {
+            aborted = true;
+            break;
+        }
+        const int a_used = s_misc[iter & 1];
+        A.head += a_used;
+        B.head += teff - a_used;
+        if (tid == 0) {
+            refill<Cfg, K, V>(A, ring, vring, bars_a, policy);
+            refill<Cfg, K, V>(B, ring + Cfg::RING, V ? vring + Cfg::RING : nullptr, bars_b, policy);
+            // C[kdone, kdone + teff) <- stage.  u = misc + k; stage slot = u - (u0 & ~3).
+            const int64_t cu0 = misc + kdone, cu1 = cu0 + teff;
+            const int64_t g0 = cu0 & ~int64_t(3);
+            const int64_t bs = (cu0 + 3) & ~int64_t(3);
+            const int64_t be = cu1 & ~int64_t(3);
+            int64_t p1 = cu1, q0 = cu1;  // plain-store intervals [cu0, p1) and [q0, cu1)
+            if (be > bs) {
+                bulk_copy_s2g(cbase16 + 4 * bs, stage_k + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
+                if (V) bulk_copy_s2g(cvbase16 + 4 * bs, stage_v + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
+                p1 = bs;
+                q0 = be;
+            }
+            K* ck = reinterpret_cast<K*>(cbase16);
+            uint32_t* cv = reinterpret_cast<uint32_t*>(cvbase16);
+            for (int64_t u = cu0; u < p1; ++u) {
+                ck[u] = stage_k[u - g0];
+                if (V) cv[u] = stage_v[u - g0];
+            }
+            for (int64_t u = q0; u < cu1; ++u) {
+                ck[u] = stage_k[u - g0];
+                if (V) cv[u] = stage_v[u - g0];
+            }
+            bulk_commit();
+        }
         kdone += teff;
-        __syncthreads();  // stage reads done before the next sub-tile writes it
     }
 
-    if (aborted && tid == 0) {
-        // Let every requested copy land (bounded) before the CTA's shared
-        // memory is released.
-        for (int side = 0; side < 2; ++side) {
-            SideStream* sp = side == 0 ? &A : &B;
-            uint64_t* bars = side == 0 ? bars_a : bars_b;
-            for (int64_t c = sp->next_wait; c < sp->next_issue; ++c) {
-                const int64_t rel = c - sp->c_first;
-                mbar_wait_bounded(&bars[rel & (Cfg::NCH - 1)], (uint32_t)(rel >> Cfg::NCH_LOG2) & 1u, err);
+    if (tid == 0) {
+        if (aborted) {
+            // Let every requested copy land (bounded) before the CTA's shared
+            // memory is released.
+            for (int side = 0; side < 2; ++side) {
+                SideStream* sp = side == 0 ? &A : &B;
+                uint64_t* bars = side == 0 ? bars_a : bars_b;
+                for (int64_t c = sp->c_first + sp->next_wait; c < sp->next_issue; ++c) {
+                    const int rel = (int)(c - sp->c_first);
+                    mbar_wait_bounded(&bars[rel & (Cfg::NCH - 1)], (uint32_t)(rel >> Cfg::NCH_LOG2) & 1u, err);
+                }
             }
         }
+        bulk_wait_all();  // the last stage stores have landed in C
     }
 }
 
