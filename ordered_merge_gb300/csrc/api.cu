@@ -16,9 +16,25 @@
 namespace om {
 
 // Kernel configurations.
-//  merge: 128 threads x 15 outputs = 1920 outputs per sub-tile; 4096-element
-//         rings per side refilled in 512-element (2 KB) chunks.
-using MergeCfg = TileCfg<128, 15, 12, 9>;
+//  merge: 128 threads x 23 outputs = 2944 outputs per sub-tile; 4096-element
+//         rings per side refilled in 1024-element (4 KB) chunks; 44 KB of
+//         shared memory, 5 CTAs per SM.  (Measured on GB300 against 1920- and
+//         2432-output sub-tiles, 512/2048-element chunks, 8192-element rings
+//         and 192/256-thread CTAs: per-sub-tile and per-chunk work dominates,
+//         so the largest sub-tile and chunk that fit a 4096 ring win.)
+using MergeCfg = TileCfg<128, 23, 12, 10>;
+//  key+value merge: four rings (keys and values of A and B), so smaller rings
+//  keep 5 CTAs per SM: 128 x 11 = 1408 outputs per sub-tile, 2048-element
+//  rings, 512-element chunks.
+using PairsCfg = TileCfg<128, 11, 11, 9>;
+template <bool V>
+struct CfgFor {
+    using type = MergeCfg;
+};
+template <>
+struct CfgFor<true> {
+    using type = PairsCfg;
+};
 //  sort: runs of 1024 from a 128 x 8 block sort; early passes merge whole
 //        pairs of runs inside 256 x 16 = 4096-element tiles; later passes use
 //        the partition + tile-merge kernels on each pair of runs.
@@ -68,7 +84,7 @@ static om_status device_state(DeviceState** out) {
         cudaError_t e = cudaSuccess;
         e = e ? e : set_smem(tile_merge_kernel<MergeCfg, int32_t, false>, TileSmem<MergeCfg, false>::total);
         e = e ? e : set_smem(tile_merge_kernel<MergeCfg, uint32_t, false>, TileSmem<MergeCfg, false>::total);
-        e = e ? e : set_smem(tile_merge_kernel<MergeCfg, uint32_t, true>, TileSmem<MergeCfg, true>::total);
+        e = e ? e : set_smem(tile_merge_kernel<PairsCfg, uint32_t, true>, TileSmem<PairsCfg, true>::total);
         e = e ? e : set_smem(block_sort_kernel<RunSortCfg, true>, block_sort_smem_bytes<RunSortCfg, true>());
         e = e ? e : set_smem(block_sort_kernel<RunSortCfg, false>, block_sort_smem_bytes<RunSortCfg, false>());
         e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, true>, block_sort_smem_bytes<SmallMergeCfg, true>());
@@ -78,8 +94,8 @@ static om_status device_state(DeviceState** out) {
                                                           tile_merge_kernel<MergeCfg, int32_t, false>, MergeCfg::NT,
                                                           TileSmem<MergeCfg, false>::total);
         e = e ? e : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge_v,
-                                                                   tile_merge_kernel<MergeCfg, uint32_t, true>,
-                                                                   MergeCfg::NT, TileSmem<MergeCfg, true>::total);
+                                                                   tile_merge_kernel<PairsCfg, uint32_t, true>,
+                                                                   PairsCfg::NT, TileSmem<PairsCfg, true>::total);
         if (e != cudaSuccess) return OM_ECUDA;
         if (d.resident_merge < 1) d.resident_merge = 1;
         if (d.resident_merge_v < 1) d.resident_merge_v = 1;
@@ -193,12 +209,13 @@ static om_status cuda_fail(cudaError_t e) {
 // slots of scratch).
 template <typename K, bool V>
 static cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const DeviceState* d, cudaStream_t st) {
-    using Smem = TileSmem<MergeCfg, V>;
-    const unsigned pgrid = (unsigned)((g.nranges + 127) / 128);
+    using Cfg = typename CfgFor<V>::type;
+    using Smem = TileSmem<Cfg, V>;
+    const unsigned pgrid = (unsigned)((g.nranges + 3) / 4);  // one warp per range
     cudaError_t e = traced(kKindPartition, st, [&] { partition_kernel<K, V><<<pgrid, 128, 0, st>>>(g, split); });
     if (e != cudaSuccess) return e;
     return traced(kKindTileMerge, st, [&] {
-        tile_merge_kernel<MergeCfg, K, V><<<(unsigned)g.nranges, MergeCfg::NT, Smem::total, st>>>(g, split, d->err);
+        tile_merge_kernel<Cfg, K, V><<<(unsigned)g.nranges, Cfg::NT, Smem::total, st>>>(g, split, d->err);
     });
 }
 
@@ -208,10 +225,11 @@ static om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K*
     DeviceState* d = nullptr;
     om_status s = device_state(&d);
     if (s != OM_OK) return s;
+    using Cfg = typename CfgFor<V>::type;
     const int64_t total = m + n;
-    const int64_t subtiles = (total + MergeCfg::T - 1) / MergeCfg::T;
+    const int64_t subtiles = (total + Cfg::T - 1) / Cfg::T;
     const int64_t resident = (int64_t)d->sm_count * (V ? d->resident_merge_v : d->resident_merge);
-    const int64_t range_len = subtiles_per_range(subtiles, resident) * MergeCfg::T;
+    const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
     const int64_t nranges = (total + range_len - 1) / range_len;
     if (nranges > 0x7fffffff) return OM_ERANGE;
     MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
@@ -236,11 +254,19 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
     // Pass schedule.  Run sort to kRunLen, then one pass per doubling.
     int passes = 0;
     for (int64_t r = kRunLen; r < n; r *= 2) ++passes;
-    const int64_t subtiles = (n + MergeCfg::T - 1) / MergeCfg::T;
+    using Cfg = typename CfgFor<V>::type;
+    const int64_t subtiles = (n + Cfg::T - 1) / Cfg::T;
     const int64_t resident = (int64_t)d->sm_count * (V ? d->resident_merge_v : d->resident_merge);
-    const int64_t range_len = subtiles_per_range(subtiles, resident) * MergeCfg::T;
-    // splitter slots for the largest late pass: ranges of every pair, plus one
-    const int64_t max_ranges = (n + range_len - 1) / range_len + (n + 2 * kRunLen - 1) / (2 * kRunLen) + 1;
+    const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
+    // splitter slots for the largest late pass (every pair gets the same
+    // number of ranges, including a short last pair), plus one
+    int64_t max_ranges = 1;
+    for (int64_t r = kRunLen; r < n; r *= 2) {
+        if (2 * r <= SmallMergeCfg::TILE) continue;
+        const int64_t npairs = (n + 2 * r - 1) / (2 * r);
+        const int64_t rps = (2 * r + range_len - 1) / range_len;
+        if (npairs * rps + 1 > max_ranges) max_ranges = npairs * rps + 1;
+    }
 
     uint32_t* tk = nullptr;
     uint32_t* tv = nullptr;
@@ -304,11 +330,6 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
     return e == cudaSuccess ? OM_OK : cuda_fail(e);
 }
 
-__global__ void corank_one_kernel(int64_t k, const int32_t* A, int64_t m, const int32_t* B, int64_t n,
-                                  int64_t* out) {
-    *out = corank_global(k, A, m, B, n);
-}
-
 }  // namespace om
 
 using namespace om;
@@ -325,7 +346,7 @@ int64_t om_corank_i32(int64_t k, const int32_t* A, int64_t m, const int32_t* B, 
     if (s != OM_OK) return -(int64_t)s;
     std::lock_guard<std::mutex> lk(g_corank_mu);
     cudaError_t e = traced(kKindCorank, (cudaStream_t)0,
-                           [&] { corank_one_kernel<<<1, 1, 0, 0>>>(k, A, m, B, n, d->corank_slot); });
+                           [&] { corank_one_kernel<int32_t><<<1, 32, 0, 0>>>(k, A, m, B, n, d->corank_slot); });
     if (e != cudaSuccess) return -(int64_t)OM_ECUDA;
     int64_t i = -1;
     if (cudaMemcpy(&i, d->corank_slot, sizeof(i), cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -469,8 +490,9 @@ uint64_t om_launch_count(void) { return g_launches.load(std::memory_order_relaxe
 // cleared between calls; but two calls whose kernels overlap on the GPU (for
 // example on two streams) race on the array and may produce wrong output.
 constexpr int64_t kNoAllocSplits = 8192;  // int64 slots: 64 KiB
-constexpr int64_t kNoAllocMaxSubtilesPerRange = 64;
-constexpr int64_t kNoAllocMaxOutputs = (kNoAllocSplits - 1) * kNoAllocMaxSubtilesPerRange * MergeCfg::T;
+// The documented limit on m + n.  Output ranges are lengthened as needed so
+// that any merge up to it needs at most kNoAllocSplits - 1 of them.
+constexpr int64_t kNoAllocMaxOutputs = 1006510080;
 
 static __device__ __align__(256) int64_t g_noalloc_splits[kNoAllocSplits];
 

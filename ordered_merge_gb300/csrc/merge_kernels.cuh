@@ -128,19 +128,60 @@ __device__ __forceinline__ int64_t corank_global(int64_t k, const K* __restrict_
     return lo;
 }
 
+// co_rank(k) by one warp, 33-way: while the interval [lo, hi] holds more
+// than 32 candidates, the 32 lanes probe 32 evenly spaced points at once and
+// a ballot keeps the sub-interval between the last probe that passed and the
+// first that failed; the last <= 32 candidates are probed in one round.  This
+// is the higher-radix form of the same search ("Co-rank Function 實作與
+// Basic Parallel Merge Kernel", §Overview: binary search, or higher radix):
+// about log33(range) + 1 rounds of parallel loads instead of log2(range)
+// dependent loads.  Every lane returns the result.  On unsorted input the
+// passing probes need not form a prefix; the interval still shrinks every
+// round, so the loop always ends.
+template <typename K>
+__device__ __forceinline__ int64_t corank_warp(int64_t k, const K* __restrict__ A, int64_t m,
+                                               const K* __restrict__ B, int64_t n, int lane) {
+    int64_t lo = k - n > 0 ? k - n : 0;
+    int64_t hi = k < m ? k : m;
+    while (hi - lo > 32) {
+        const int64_t span = hi - lo;
+        const int64_t c = lo + (span * (lane + 1)) / 33;  // lo < c < hi
+        const bool pass = __ldg(A + c - 1) <= __ldg(B + k - c);
+        const int t = __popc(__ballot_sync(0xffffffffu, pass));
+        const int64_t new_lo = (t == 0) ? lo : lo + (span * t) / 33;
+        const int64_t new_hi = (t == 32) ? hi : lo + (span * (t + 1)) / 33 - 1;
+        lo = new_lo;
+        hi = new_hi;
+    }
+    const int64_t c = lo + 1 + lane;
+    bool pass = false;
+    if (c <= hi) pass = __ldg(A + c - 1) <= __ldg(B + k - c);
+    return lo + __popc(__ballot_sync(0xffffffffu, pass));
+}
+
 // Partition kernel: split[r] = co-rank of the first output of range r within
-// its segment.  One thread per range.
+// its segment.  One warp per range.
 template <typename K, bool V>
 __global__ void __launch_bounds__(128) partition_kernel(MergeGeom<K> g, int64_t* __restrict__ split) {
-    const int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (r >= g.nranges) return;
+    const int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= g.nranges) return;  // whole warp
     const int64_t seg = r / g.ranges_per_seg;
     const int64_t local = r - seg * g.ranges_per_seg;
     const Segment<K> s = segment_of<K, V>(g, seg);
     const int64_t len = s.m + s.n;
     int64_t k = local * g.range_len;
     if (k > len) k = len;
-    split[r] = corank_global(k, s.ak, s.m, s.bk, s.n);
+    const int64_t i = corank_warp(k, s.ak, s.m, s.bk, s.n, lane);
+    if (lane == 0) split[r] = i;
+}
+
+// One co-rank by one warp.
+template <typename K>
+__global__ void __launch_bounds__(32) corank_one_kernel(int64_t k, const K* __restrict__ A, int64_t m,
+                                                        const K* __restrict__ B, int64_t n, int64_t* out) {
+    const int64_t i = corank_warp(k, A, m, B, n, threadIdx.x & 31);
+    if (threadIdx.x == 0) *out = i;
 }
 
 // Batched co-rank of one merge (device ks -> device i).
