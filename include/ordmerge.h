@@ -146,8 +146,9 @@ uint64_t om_launch_count(void);
  * in full by another allocator, so that a stream-ordered allocation could
  * fail, and code with latency bounds that must not enter an allocator.
  *
- *  - m + n may be at most 1,006,510,080 (8191 ranges of 64 sub-tiles of 1920
- *    outputs); larger merges return OM_ERANGE and launch nothing.
+ *  - m + n may be at most 1,006,510,080 (the array holds 8191 output-range
+ *    splitters; ranges are lengthened as needed to fit); larger merges return
+ *    OM_ERANGE and launch nothing.
  *  - The first call on each device does a one-time set-up there (it looks up
  *    the array's device address and sets kernel attributes); make that first
  *    call before any stream capture.

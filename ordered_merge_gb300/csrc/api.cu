@@ -15,18 +15,19 @@
 
 namespace om {
 
-// Kernel configurations.
-//  merge: 128 threads x 23 outputs = 2944 outputs per sub-tile; 4096-element
-//         rings per side refilled in 1024-element (4 KB) chunks; 44 KB of
+// Kernel configurations (consumer threads, outputs per thread, log2 ring,
+// log2 chunk; every CTA has one more warp for the producer).
+//  merge: 128 consumers x 23 outputs = 2944 outputs per sub-tile; 4096-element
+//         rings per side refilled in 1024-element (4 KB) chunks; 45 KB of
 //         shared memory, 5 CTAs per SM.  (Measured on GB300 against 1920- and
 //         2432-output sub-tiles, 512/2048-element chunks, 8192-element rings
-//         and 192/256-thread CTAs: per-sub-tile and per-chunk work dominates,
-//         so the largest sub-tile and chunk that fit a 4096 ring win.)
+//         and 64- to 256-thread CTAs: per-sub-tile and per-chunk work
+//         dominates, so the largest sub-tile and chunk that fit a 4096 ring win.)
 using MergeCfg = TileCfg<128, 23, 12, 10>;
 //  key+value merge: four rings (keys and values of A and B), so smaller rings
-//  keep 5 CTAs per SM: 128 x 11 = 1408 outputs per sub-tile, 2048-element
-//  rings, 512-element chunks.
-using PairsCfg = TileCfg<128, 11, 11, 9>;
+//  keep 5 CTAs per SM: 96 x 15 = 1440 outputs per sub-tile, 2048-element
+//  rings, 512-element chunks (best of eight shapes measured on GB300).
+using PairsCfg = TileCfg<96, 15, 11, 9>;
 template <bool V>
 struct CfgFor {
     using type = MergeCfg;
@@ -91,11 +92,11 @@ static om_status device_state(DeviceState** out) {
         e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, false>, block_sort_smem_bytes<SmallMergeCfg, false>());
         if (e != cudaSuccess) return OM_ECUDA;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge,
-                                                          tile_merge_kernel<MergeCfg, int32_t, false>, MergeCfg::NT,
-                                                          TileSmem<MergeCfg, false>::total);
+                                                          tile_merge_kernel<MergeCfg, int32_t, false>,
+                                                          MergeCfg::NT + 32, TileSmem<MergeCfg, false>::total);
         e = e ? e : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge_v,
                                                                    tile_merge_kernel<PairsCfg, uint32_t, true>,
-                                                                   PairsCfg::NT, TileSmem<PairsCfg, true>::total);
+                                                                   PairsCfg::NT + 32, TileSmem<PairsCfg, true>::total);
         if (e != cudaSuccess) return OM_ECUDA;
         if (d.resident_merge < 1) d.resident_merge = 1;
         if (d.resident_merge_v < 1) d.resident_merge_v = 1;
@@ -215,9 +216,14 @@ static cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const Dev
     cudaError_t e = traced(kKindPartition, st, [&] { partition_kernel<K, V><<<pgrid, 128, 0, st>>>(g, split); });
     if (e != cudaSuccess) return e;
     return traced(kKindTileMerge, st, [&] {
-        tile_merge_kernel<Cfg, K, V><<<(unsigned)g.nranges, Cfg::NT, Smem::total, st>>>(g, split, d->err);
+        tile_merge_kernel<Cfg, K, V><<<(unsigned)g.nranges, Cfg::NT + 32, Smem::total, st>>>(g, split, d->err);
     });
 }
+
+
+
+
+
 
 template <typename K, bool V>
 static om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, const uint32_t* bv,

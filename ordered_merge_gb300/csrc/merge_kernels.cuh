@@ -16,21 +16,25 @@
 //
 // GB300 design (what differs from the pages):
 //  * The grid-level co-rank is a separate partition kernel that writes one
-//    splitter per output range (the pages' thread 0 search per block).
-//  * The search is the bounded bisection form of the same co-rank: the
-//    largest i in [max(0,k-n), min(k,m)] with i == lower bound or
-//    A[i-1] <= B[k-i].  On sorted input it is the pages' i; on any input it
-//    stops after ceil(log2(range + 1)) steps.
+//    splitter per output range (instead of thread 0 of every block), each
+//    found by one warp probing 32 points per round (higher radix).
+//  * Every search is a bounded form of the same co-rank: the largest i in
+//    [max(0,k-n), min(k,m)] with i == lower bound or A[i-1] <= B[k-i].  On
+//    sorted input it is the pages' i; on any input it stops.
 //  * Ring slots are indexed by the element's 16-byte-aligned address
-//    position (u), so every refill is a 16-byte-aligned 1-D bulk copy issued
-//    by one thread on the TMA engine and tracked by an mbarrier; the ring
-//    size is a power of two so the pages' "% tile_size" wrap is a mask.
+//    position (u), so every refill is a 16-byte-aligned 1-D bulk copy on the
+//    TMA engine tracked by an mbarrier; the ring size is a power of two so
+//    the pages' "% tile_size" wrap is a mask.
 //  * Refills run ahead: a chunk is requested as soon as the slots it lands
-//    in are consumed, so several sub-tiles of input are in flight while the
+//    in are consumed, so input for later sub-tiles is in flight while the
 //    current one is merged.
-//  * Each thread merges VT (odd) outputs into registers; they pass through a
-//    shared-memory stage so C is written with coalesced 128-bit streaming
-//    stores instead of the pages' per-thread strided writes.
+//  * The kernel is warp-specialised: one producer thread owns all bulk
+//    copies and the consumed-count bookkeeping; consumer warps only search,
+//    merge and stage, synchronised with the producer by mbarriers.
+//  * Each consumer thread merges VT (odd) outputs into registers; they pass
+//    through a shared-memory stage that the producer writes to C with one
+//    bulk store per sub-tile, instead of the pages' per-thread strided
+//    writes.
 #pragma once
 
 #include <cstdint>
@@ -215,22 +219,12 @@ struct TileCfg {
     // largest power of two <= T: the first step of the fixed-step search
     static constexpr int SEARCH_TOP = (T >= 4096) ? 4096 : (T >= 2048) ? 2048 : (T >= 1024) ? 1024
                                     : (T >= 512) ? 512 : (T >= 256) ? 256 : 128;
-    static_assert(VT % 2 == 1, "odd VT keeps the register->stage writes free of bank conflicts");
+    static_assert(VT % 2 == 1, "an odd VT keeps the register->stage writes and the search's first probes free "
+                               "of bank conflicts");
     static_assert(T % 4 == 0, "sub-tile boundaries stay 16-byte aligned in C");
     static_assert(T + CH <= RING, "a window of T plus one chunk must fit in the ring");
     static_assert(CH >= 4 && NCH >= 2, "chunks are whole 16-byte groups");
     static_assert(2 * SEARCH_TOP > T, "the fixed-step search must reach every co-rank");
-};
-
-// Shared memory: keys of both rings back to back (A ring, then B ring, so one
-// masked index addresses either), values likewise, the output stage, the
-// chunk barriers of both sides, the stage barrier and two broadcast words.
-template <typename Cfg, bool V>
-struct TileSmem {
-    static constexpr size_t ring_bytes = (size_t)2 * Cfg::RING * 4 * (V ? 2 : 1);
-    static constexpr size_t stage_bytes = (size_t)Cfg::STAGE * 4 * (V ? 2 : 1);
-    static constexpr size_t bar_bytes = (size_t)(2 * Cfg::NCH + 1) * 8;
-    static constexpr size_t total = ring_bytes + stage_bytes + bar_bytes + 16;
 };
 
 // Streaming state of one input side (A or B) of one CTA's output range.
@@ -412,30 +406,55 @@ __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, 
     return ai - ha;
 }
 
-// The tile-merge kernel.  CTA r merges output range r of the geometry:
+// Shared memory of the tile-merge kernel: keys of both rings back to back
+// (A ring, then B ring, so one masked index addresses either), values
+// likewise, the output stage, the chunk barriers of both sides, the
+// producer/consumer barriers and the per-sub-tile window descriptors.
+template <typename Cfg, bool V>
+struct TileSmem {
+    static constexpr size_t ring_bytes = (size_t)2 * Cfg::RING * 4 * (V ? 2 : 1);
+    static constexpr size_t stage_bytes = (size_t)Cfg::STAGE * 4 * (V ? 2 : 1);
+    // chunk barriers of A and B, ready[2], done[2], stage_free
+    static constexpr size_t bar_bytes = (size_t)(2 * Cfg::NCH + 5) * 8;
+    // window descriptors: 2 x {ha, hb, wa, wb, teff, pad...} ints, a_used[2], abort
+    static constexpr size_t info_bytes = 2 * 8 * 4 + 4 * 4;
+    static constexpr size_t total = ring_bytes + stage_bytes + bar_bytes + info_bytes;
+};
+
+// The tile-merge kernel.  CTA r merges output range r of the geometry,
 // C[k0, k1) from A[i0, i1) and B[j0, j1), where i0 / i1 come from the
-// partition kernel.  It walks the range in sub-tiles of T outputs:
-//   wait for the window chunks -> per-thread co-rank in the ring -> serial
-//   merge of VT outputs into registers -> stage -> one barrier -> advance the
-//   A/B heads by the sub-tile's co-rank and request the freed chunks ->
-//   bulk store of the stage to C (thread 0, asynchronous).
+// partition kernel, in sub-tiles of T outputs.  It is warp-specialised: NT
+// consumer threads merge, one producer thread (in an extra warp) owns every
+// bulk copy.  Per sub-tile s:
+//   producer: wait for the window's chunks -> publish the window (ready[s])
+//             -> wait for the consumers (done[s]) -> advance the heads by the
+//             sub-tile's co-rank, request freed chunks, bulk-store the stage
+//             -> once that store has read the stage, release it (stage_free)
+//   consumers: wait ready[s] -> co-rank + serial merge -> wait stage_free
+//             (s-1) -> write the stage -> arrive done[s]
+// Consumers never run a CTA-wide barrier and keep no streaming state.
 template <typename Cfg, typename K, bool V>
-__global__ void __launch_bounds__(Cfg::NT) tile_merge_kernel(MergeGeom<K> g, const int64_t* __restrict__ split,
-                                                             uint32_t* err) {
+__global__ void __launch_bounds__(Cfg::NT + 32) tile_merge_kernel(MergeGeom<K> g,
+                                                                    const int64_t* __restrict__ split,
+                                                                    uint32_t* err) {
     constexpr int NT = Cfg::NT;
     constexpr int VT = Cfg::VT;
     constexpr int T = Cfg::T;
     using Smem = TileSmem<Cfg, V>;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    K* ring = reinterpret_cast<K*>(smem);                       // [A ring | B ring]
+    K* ring = reinterpret_cast<K*>(smem);
     uint32_t* vring = V ? reinterpret_cast<uint32_t*>(ring + 2 * Cfg::RING) : nullptr;
     K* stage_k = reinterpret_cast<K*>(smem + Smem::ring_bytes);
     uint32_t* stage_v = V ? reinterpret_cast<uint32_t*>(stage_k + Cfg::STAGE) : nullptr;
     uint64_t* bars_a = reinterpret_cast<uint64_t*>(smem + Smem::ring_bytes + Smem::stage_bytes);
     uint64_t* bars_b = bars_a + Cfg::NCH;
-    uint64_t* bar_stage = bars_b + Cfg::NCH;
-    int* s_misc = reinterpret_cast<int*>(bar_stage + 1);  // [0], [1] a_used by parity; [2] abort
+    uint64_t* ready = bars_b + Cfg::NCH;  // [2]
+    uint64_t* done = ready + 2;          // [2]
+    uint64_t* stage_free = done + 2;     // [1]
+    int* info = reinterpret_cast<int*>(stage_free + 1);  // [2][8]: ha, hb, wa, wb, teff
+    int* a_used_slot = info + 16;                        // [2]
+    volatile int* abort_flag = info + 18;
 
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
@@ -444,7 +463,7 @@ __global__ void __launch_bounds__(Cfg::NT) tile_merge_kernel(MergeGeom<K> g, con
     const Segment<K> s = segment_of<K, V>(g, seg);
     const int64_t len = s.m + s.n;
     const int64_t k0 = local * g.range_len;
-    if (k0 >= len) return;  // whole CTA: empty range of a short last segment
+    if (k0 >= len) return;  // whole CTA
     const int64_t k1 = (k0 + g.range_len < len) ? k0 + g.range_len : len;
     const int64_t i0 = split[r];
     const int64_t i1 = (k1 == len) ? s.m : split[r + 1];
@@ -453,97 +472,64 @@ __global__ void __launch_bounds__(Cfg::NT) tile_merge_kernel(MergeGeom<K> g, con
         if (tid == 0) atomicOr(err, kErrBadRange);
         return;  // whole CTA
     }
-
-    SideStream A, B;
-    side_init<Cfg>(A, s.ak, s.av, s.m, i0, i1);
-    side_init<Cfg>(B, s.bk, s.bv, s.n, j0, j1);
+    const int nsub = (int)((k1 - k0 + T - 1) / T);
     const uintptr_t caddr = reinterpret_cast<uintptr_t>(s.ck);
-    const int64_t misc = (int64_t)((caddr >> 2) & 3);
-    char* cbase16 = reinterpret_cast<char*>(caddr & ~uintptr_t(15));
-    char* cvbase16 = V ? reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(s.cv) & ~uintptr_t(15)) : nullptr;
+    const int misc = (int)((caddr >> 2) & 3);
 
-    uint64_t policy = 0;
     if (tid == 0) {
         for (int c = 0; c < Cfg::NCH; ++c) {
             mbar_init(&bars_a[c], 1);
             mbar_init(&bars_b[c], 1);
         }
-        mbar_init(bar_stage, 1);
+        mbar_init(&ready[0], 1);
+        mbar_init(&ready[1], 1);
+        mbar_init(&done[0], NT);
+        mbar_init(&done[1], NT);
+        mbar_init(stage_free, 1);
         fence_barrier_init();
-        s_misc[2] = 0;
-        policy = l2_policy_evict_first();
+        *abort_flag = 0;
     }
-    __syncthreads();
-    if (tid == 0) {
+    __syncthreads();  // the last CTA-wide barrier: barriers initialised
+
+    if (tid >= NT) {
+        // ------------------------------------------------------ producer --
+        if (tid != NT) return;
+        SideStream A, B;
+        side_init<Cfg>(A, s.ak, s.av, s.m, i0, i1);
+        side_init<Cfg>(B, s.bk, s.bv, s.n, j0, j1);
+        char* cbase16 = reinterpret_cast<char*>(caddr & ~uintptr_t(15));
+        char* cvbase16 = V ? reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(s.cv) & ~uintptr_t(15)) : nullptr;
+        const uint64_t policy = l2_policy_evict_first();
         refill<Cfg, K, V>(A, ring, vring, bars_a, policy);
         refill<Cfg, K, V>(B, ring + Cfg::RING, V ? vring + Cfg::RING : nullptr, bars_b, policy);
-    }
-
-    bool aborted = false;
-    int iter = 0;
-    for (int64_t kdone = k0; kdone < k1; ++iter) {
-        const int teff = (int)((k1 - kdone) < T ? (k1 - kdone) : T);
-        const int wa = (int)((A.u_hi - A.head) < T ? (A.u_hi - A.head) : T);
-        const int wb = (int)((B.u_hi - B.head) < T ? (B.u_hi - B.head) : T);
-        bool ok = wait_window<Cfg>(A, A.head + wa, bars_a, err);
-        ok = wait_window<Cfg>(B, B.head + wb, bars_b, err) && ok;
-        if (!ok) s_misc[2] = 1;
-
-        const uint32_t ha = (uint32_t)A.head & Cfg::RMASK;
-        const uint32_t hb = (uint32_t)B.head & Cfg::RMASK;
-        const int d = (tid * VT < teff) ? tid * VT : teff;
-        K keys[VT];
-        uint32_t vals[VT];
-        const bool full = (teff == T) && (wa == T) && (wb == T);  // uniform across the CTA
-        int cnt = VT;
-        uint32_t apos;
-        if (full) {
-            const int a = corank_ring<Cfg, K>(d, 0, d, ring, ha, hb);
-            apos = merge_serial<Cfg, K, V, false>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
-        } else {
-            cnt = (teff - d < VT) ? teff - d : VT;
-            const int lo = d - wb > 0 ? d - wb : 0;
-            const int hi = d < wa ? d : wa;
-            const int a = corank_ring<Cfg, K>(d, lo, hi, ring, ha, hb);
-            apos = merge_serial<Cfg, K, V, true>(a, d - a, cnt, wa, wb, ring, vring, ha, hb, keys, vals);
-        }
-        if (tid == NT - 1) s_misc[iter & 1] = (int)apos;  // = co_rank(teff): A elements this sub-tile used
-
-        // The stage is free once the bulk store of the previous sub-tile has
-        // read it: thread 0 waits for that and arrives on the stage barrier.
-        if (iter > 0) {
-            if (tid == 0) {
-                bulk_wait_read_all();
-                mbar_arrive(bar_stage);
+        int64_t kdone = k0;
+        bool failed = false;
+        for (int it = 0; it < nsub; ++it) {
+            const int teff = (int)((k1 - kdone) < T ? (k1 - kdone) : T);
+            const int wa = (int)((A.u_hi - A.head) < T ? (A.u_hi - A.head) : T);
+            const int wb = (int)((B.u_hi - B.head) < T ? (B.u_hi - B.head) : T);
+            bool ok = wait_window<Cfg>(A, A.head + wa, bars_a, err);
+            ok = wait_window<Cfg>(B, B.head + wb, bars_b, err) && ok;
+            int* inf = info + 8 * (it & 1);
+            inf[0] = (int)((uint32_t)A.head & Cfg::RMASK);
+            inf[1] = (int)((uint32_t)B.head & Cfg::RMASK);
+            inf[2] = wa;
+            inf[3] = wb;
+            inf[4] = teff;
+            if (!ok) *abort_flag = 1;
+            mbar_arrive(&ready[it & 1]);  // release: window data and descriptor
+            if (it > 0) {
+                bulk_wait_read_all();  // the previous sub-tile's store has read the stage
+                mbar_arrive(stage_free);
             }
-            if (!mbar_wait_bounded(bar_stage, (uint32_t)(iter - 1) & 1u, err)) s_misc[2] = 1;
-        }
-        const int off = (int)misc;  // stage slot of output k is k - kdone + (misc + kdone) % 4
-        if (full) {
-#pragma unroll
-            for (int v = 0; v < VT; ++v) {
-                stage_k[off + d + v] = keys[v];
-                if (V) stage_v[off + d + v] = vals[v];
+            if (!ok || !mbar_wait_bounded(&done[it & 1], (uint32_t)(it >> 1) & 1u, err)) {
+                *abort_flag = 1;
+                failed = true;
+                break;
             }
-        } else {
-#pragma unroll
-            for (int v = 0; v < VT; ++v) {
-                if (v < cnt) {
-                    stage_k[off + d + v] = keys[v];
-                    if (V) stage_v[off + d + v] = vals[v];
-                }
-            }
-        }
-        fence_proxy_async_smem();  // stage writes -> visible to the bulk store
-        __syncthreads();           // ring reads done, stage written, a_used published
-        if (s_misc[2]) {
-            aborted = true;
-            break;
-        }
-        const int a_used = s_misc[iter & 1];
-        A.head += a_used;
-        B.head += teff - a_used;
-        if (tid == 0) {
+            const int a_used = a_used_slot[it & 1];
+            A.head += a_used;
+            B.head += teff - a_used;
             refill<Cfg, K, V>(A, ring, vring, bars_a, policy);
             refill<Cfg, K, V>(B, ring + Cfg::RING, V ? vring + Cfg::RING : nullptr, bars_b, policy);
             // C[kdone, kdone + teff) <- stage.  u = misc + k; stage slot = u - (u0 & ~3).
@@ -551,7 +537,7 @@ __global__ void __launch_bounds__(Cfg::NT) tile_merge_kernel(MergeGeom<K> g, con
             const int64_t g0 = cu0 & ~int64_t(3);
             const int64_t bs = (cu0 + 3) & ~int64_t(3);
             const int64_t be = cu1 & ~int64_t(3);
-            int64_t p1 = cu1, q0 = cu1;  // plain-store intervals [cu0, p1) and [q0, cu1)
+            int64_t p1 = cu1, q0 = cu1;
             if (be > bs) {
                 bulk_copy_s2g(cbase16 + 4 * bs, stage_k + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
                 if (V) bulk_copy_s2g(cvbase16 + 4 * bs, stage_v + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
@@ -569,24 +555,76 @@ __global__ void __launch_bounds__(Cfg::NT) tile_merge_kernel(MergeGeom<K> g, con
                 if (V) cv[u] = stage_v[u - g0];
             }
             bulk_commit();
+            kdone += teff;
         }
-        kdone += teff;
-    }
-
-    if (tid == 0) {
-        if (aborted) {
-            // Let every requested copy land (bounded) before the CTA's shared
-            // memory is released.
+        if (failed) {
+            // Let every requested chunk land (bounded) before the CTA's shared
+            // memory is released; only the last NCH requests can be pending.
             for (int side = 0; side < 2; ++side) {
                 SideStream* sp = side == 0 ? &A : &B;
                 uint64_t* bars = side == 0 ? bars_a : bars_b;
-                for (int64_t c = sp->c_first + sp->next_wait; c < sp->next_issue; ++c) {
+                const int64_t c0 = sp->next_issue - Cfg::NCH > sp->c_first ? sp->next_issue - Cfg::NCH : sp->c_first;
+                for (int64_t c = c0; c < sp->next_issue; ++c) {
                     const int rel = (int)(c - sp->c_first);
                     mbar_wait_bounded(&bars[rel & (Cfg::NCH - 1)], (uint32_t)(rel >> Cfg::NCH_LOG2) & 1u, err);
                 }
             }
         }
-        bulk_wait_all();  // the last stage stores have landed in C
+        bulk_wait_all();
+        return;
+    }
+
+    // -------------------------------------------------------- consumers --
+    const int dthr = tid * VT;
+    for (int it = 0; it < nsub; ++it) {
+        if (!mbar_wait_bounded(&ready[it & 1], (uint32_t)(it >> 1) & 1u, err) || *abort_flag) {
+            *abort_flag = 1;
+            return;
+        }
+        const int* inf = info + 8 * (it & 1);
+        const uint32_t ha = (uint32_t)inf[0];
+        const uint32_t hb = (uint32_t)inf[1];
+        const int wa = inf[2];
+        const int wb = inf[3];
+        const int teff = inf[4];
+        const int d = dthr < teff ? dthr : teff;
+        K keys[VT];
+        uint32_t vals[VT];
+        const bool full = (teff == T) && (wa == T) && (wb == T);
+        int cnt = VT;
+        uint32_t apos;
+        if (full) {
+            const int a = corank_ring<Cfg, K>(d, 0, d, ring, ha, hb);
+            apos = merge_serial<Cfg, K, V, false>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
+        } else {
+            cnt = (teff - d < VT) ? teff - d : VT;
+            const int lo = d - wb > 0 ? d - wb : 0;
+            const int hi = d < wa ? d : wa;
+            const int a = corank_ring<Cfg, K>(d, lo, hi, ring, ha, hb);
+            apos = merge_serial<Cfg, K, V, true>(a, d - a, cnt, wa, wb, ring, vring, ha, hb, keys, vals);
+        }
+        if (it > 0 && !mbar_wait_bounded(stage_free, (uint32_t)(it - 1) & 1u, err)) {
+            *abort_flag = 1;
+            return;
+        }
+        if (full) {
+#pragma unroll
+            for (int v = 0; v < VT; ++v) {
+                stage_k[misc + d + v] = keys[v];
+                if (V) stage_v[misc + d + v] = vals[v];
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < VT; ++v) {
+                if (v < cnt) {
+                    stage_k[misc + d + v] = keys[v];
+                    if (V) stage_v[misc + d + v] = vals[v];
+                }
+            }
+        }
+        fence_proxy_async_smem();  // stage writes -> visible to the bulk store
+        if (tid == NT - 1) a_used_slot[it & 1] = (int)apos;  // = co_rank(teff)
+        mbar_arrive(&done[it & 1]);                          // release: stage, a_used, ring reads done
     }
 }
 
