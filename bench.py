@@ -461,8 +461,9 @@ def bench_reference(args):
     import synth
 
     lib = oracle.load()
-    # per-step sample: same recipe, scaled so all K + W steps take ~60 s
-    budget_s = 60.0
+    # per-step sample: same recipe, scaled so all K + W steps take about
+    # --ref-budget-s seconds on one core
+    budget_s = float(args.ref_budget_s)
     rate_guess = 2.5e8
     per_step = budget_s * rate_guess / max(1, args.steps + args.warmup)
     scale = 0
@@ -517,6 +518,8 @@ def main(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--ref-budget-s", type=float, default=60.0,
+                   help="reference arm: CPU seconds the K + W oracle steps should take in total")
     p.add_argument("--scale-log2", type=int, default=0,
                    help="shrink the workload by 2^-s (profiling small cases; 0 = the named size)")
     args = p.parse_args(argv)

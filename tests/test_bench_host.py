@@ -17,8 +17,8 @@ import bench  # noqa: E402
 
 def test_reference_arm_line():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=600,
-                         env={**os.environ, "RANK": "0", "WORLD_SIZE": "1"})
+                          "--steps", "3", "--warmup", "3", "--ref-budget-s", "0.5"], capture_output=True,
+                         text=True, timeout=600, env={**os.environ, "RANK": "0", "WORLD_SIZE": "1"})
     assert out.returncode == 0, out.stderr
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
