@@ -16,7 +16,7 @@
 namespace om {
 
 // Kernel configurations (consumer threads, outputs per thread, log2 ring,
-// log2 chunk; every CTA has one more warp for the producer).
+// log2 chunk; every CTA has two more warps for the producers).
 //  merge: 128 consumers x 23 outputs = 2944 outputs per sub-tile; 4096-element
 //         rings per side refilled in 1024-element (4 KB) chunks; 45 KB of
 //         shared memory, 5 CTAs per SM.  (Measured on GB300 against 1920- and
@@ -93,10 +93,10 @@ static om_status device_state(DeviceState** out) {
         if (e != cudaSuccess) return OM_ECUDA;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge,
                                                           tile_merge_kernel<MergeCfg, int32_t, false>,
-                                                          MergeCfg::NT + 32, TileSmem<MergeCfg, false>::total);
+                                                          MergeCfg::THREADS, TileSmem<MergeCfg, false>::total);
         e = e ? e : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge_v,
                                                                    tile_merge_kernel<PairsCfg, uint32_t, true>,
-                                                                   PairsCfg::NT + 32, TileSmem<PairsCfg, true>::total);
+                                                                   PairsCfg::THREADS, TileSmem<PairsCfg, true>::total);
         if (e != cudaSuccess) return OM_ECUDA;
         if (d.resident_merge < 1) d.resident_merge = 1;
         if (d.resident_merge_v < 1) d.resident_merge_v = 1;
@@ -216,7 +216,7 @@ static cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const Dev
     cudaError_t e = traced(kKindPartition, st, [&] { partition_kernel<K, V><<<pgrid, 128, 0, st>>>(g, split); });
     if (e != cudaSuccess) return e;
     return traced(kKindTileMerge, st, [&] {
-        tile_merge_kernel<Cfg, K, V><<<(unsigned)g.nranges, Cfg::NT + 32, Smem::total, st>>>(g, split, d->err);
+        tile_merge_kernel<Cfg, K, V><<<(unsigned)g.nranges, Cfg::THREADS, Smem::total, st>>>(g, split, d->err);
     });
 }
 

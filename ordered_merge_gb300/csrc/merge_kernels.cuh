@@ -28,11 +28,12 @@
 //  * Refills run ahead: a chunk is requested as soon as the slots it lands
 //    in are consumed, so input for later sub-tiles is in flight while the
 //    current one is merged.
-//  * The kernel is warp-specialised: one producer thread owns all bulk
-//    copies and the consumed-count bookkeeping; consumer warps only search,
-//    merge and stage, synchronised with the producer by mbarriers.
+//  * The kernel is warp-specialised: two producer threads (one per input
+//    side) own all bulk copies and the consumed-count bookkeeping; consumer
+//    warps only search, merge and stage, synchronised with the producers by
+//    mbarriers.
 //  * Each consumer thread merges VT (odd) outputs into registers; they pass
-//    through a shared-memory stage that the producer writes to C with one
+//    through a shared-memory stage that a producer writes to C with one
 //    bulk store per sub-tile, instead of the pages' per-thread strided
 //    writes.
 #pragma once
@@ -205,7 +206,8 @@ __global__ void __launch_bounds__(128) corank_batch_kernel(const int64_t* __rest
 
 template <int NT_, int VT_, int RING_LOG2_, int CH_LOG2_>
 struct TileCfg {
-    static constexpr int NT = NT_;
+    static constexpr int NT = NT_;          // consumer threads
+    static constexpr int THREADS = NT + 64;  // plus two producer warps
     static constexpr int VT = VT_;
     static constexpr int T = NT * VT;  // outputs per sub-tile
     static constexpr int RING_LOG2 = RING_LOG2_;
@@ -424,17 +426,18 @@ struct TileSmem {
 // The tile-merge kernel.  CTA r merges output range r of the geometry,
 // C[k0, k1) from A[i0, i1) and B[j0, j1), where i0 / i1 come from the
 // partition kernel, in sub-tiles of T outputs.  It is warp-specialised: NT
-// consumer threads merge, one producer thread (in an extra warp) owns every
-// bulk copy.  Per sub-tile s:
-//   producer: wait for the window's chunks -> publish the window (ready[s])
-//             -> wait for the consumers (done[s]) -> advance the heads by the
-//             sub-tile's co-rank, request freed chunks, bulk-store the stage
-//             -> once that store has read the stage, release it (stage_free)
+// consumer threads merge; two producer threads (lane 0 of two extra warps)
+// own the bulk copies, one per input side.  Per sub-tile s:
+//   producers: wait for the side's window chunks -> publish it (ready[s],
+//             count 2) -> wait for the consumers (done[s]) -> advance the
+//             side's head by the sub-tile's co-rank, request freed chunks;
+//             the A producer also bulk-stores the stage and, once that store
+//             has read it, releases it (stage_free)
 //   consumers: wait ready[s] -> co-rank + serial merge -> wait stage_free
 //             (s-1) -> write the stage -> arrive done[s]
 // Consumers never run a CTA-wide barrier and keep no streaming state.
 template <typename Cfg, typename K, bool V>
-__global__ void __launch_bounds__(Cfg::NT + 32) tile_merge_kernel(MergeGeom<K> g,
+__global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g,
                                                                     const int64_t* __restrict__ split,
                                                                     uint32_t* err) {
     constexpr int NT = Cfg::NT;
@@ -481,8 +484,8 @@ __global__ void __launch_bounds__(Cfg::NT + 32) tile_merge_kernel(MergeGeom<K> g
             mbar_init(&bars_a[c], 1);
             mbar_init(&bars_b[c], 1);
         }
-        mbar_init(&ready[0], 1);
-        mbar_init(&ready[1], 1);
+        mbar_init(&ready[0], 2);  // both producers
+        mbar_init(&ready[1], 2);
         mbar_init(&done[0], NT);
         mbar_init(&done[1], NT);
         mbar_init(stage_free, 1);
@@ -492,33 +495,38 @@ __global__ void __launch_bounds__(Cfg::NT + 32) tile_merge_kernel(MergeGeom<K> g
     __syncthreads();  // the last CTA-wide barrier: barriers initialised
 
     if (tid >= NT) {
-        // ------------------------------------------------------ producer --
-        if (tid != NT) return;
-        SideStream A, B;
-        side_init<Cfg>(A, s.ak, s.av, s.m, i0, i1);
-        side_init<Cfg>(B, s.bk, s.bv, s.n, j0, j1);
+        // ----------------------------------------------------- producers --
+        // Lane 0 of each extra warp: the first streams A, the second B, so
+        // the two sides' refills and chunk waits run side by side.  The A
+        // producer also owns the stage: it bulk-stores it and hands it back.
+        if ((tid & 31) != 0) return;
+        const bool side_a = tid == NT;
+        SideStream S;
+        if (side_a) {
+            side_init<Cfg>(S, s.ak, s.av, s.m, i0, i1);
+        } else {
+            side_init<Cfg>(S, s.bk, s.bv, s.n, j0, j1);
+        }
+        K* rk = side_a ? ring : ring + Cfg::RING;
+        uint32_t* rv = V ? (side_a ? vring : vring + Cfg::RING) : nullptr;
+        uint64_t* bars = side_a ? bars_a : bars_b;
         char* cbase16 = reinterpret_cast<char*>(caddr & ~uintptr_t(15));
         char* cvbase16 = V ? reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(s.cv) & ~uintptr_t(15)) : nullptr;
         const uint64_t policy = l2_policy_evict_first();
-        refill<Cfg, K, V>(A, ring, vring, bars_a, policy);
-        refill<Cfg, K, V>(B, ring + Cfg::RING, V ? vring + Cfg::RING : nullptr, bars_b, policy);
+        refill<Cfg, K, V>(S, rk, rv, bars, policy);
         int64_t kdone = k0;
         bool failed = false;
         for (int it = 0; it < nsub; ++it) {
             const int teff = (int)((k1 - kdone) < T ? (k1 - kdone) : T);
-            const int wa = (int)((A.u_hi - A.head) < T ? (A.u_hi - A.head) : T);
-            const int wb = (int)((B.u_hi - B.head) < T ? (B.u_hi - B.head) : T);
-            bool ok = wait_window<Cfg>(A, A.head + wa, bars_a, err);
-            ok = wait_window<Cfg>(B, B.head + wb, bars_b, err) && ok;
+            const int w = (int)((S.u_hi - S.head) < T ? (S.u_hi - S.head) : T);
+            const bool ok = wait_window<Cfg>(S, S.head + w, bars, err);
             int* inf = info + 8 * (it & 1);
-            inf[0] = (int)((uint32_t)A.head & Cfg::RMASK);
-            inf[1] = (int)((uint32_t)B.head & Cfg::RMASK);
-            inf[2] = wa;
-            inf[3] = wb;
-            inf[4] = teff;
+            inf[side_a ? 0 : 1] = (int)((uint32_t)S.head & Cfg::RMASK);
+            inf[side_a ? 2 : 3] = w;
+            if (side_a) inf[4] = teff;
             if (!ok) *abort_flag = 1;
-            mbar_arrive(&ready[it & 1]);  // release: window data and descriptor
-            if (it > 0) {
+            mbar_arrive(&ready[it & 1]);  // release: this side's window and descriptor
+            if (side_a && it > 0) {
                 bulk_wait_read_all();  // the previous sub-tile's store has read the stage
                 mbar_arrive(stage_free);
             }
@@ -528,49 +536,45 @@ __global__ void __launch_bounds__(Cfg::NT + 32) tile_merge_kernel(MergeGeom<K> g
                 break;
             }
             const int a_used = a_used_slot[it & 1];
-            A.head += a_used;
-            B.head += teff - a_used;
-            refill<Cfg, K, V>(A, ring, vring, bars_a, policy);
-            refill<Cfg, K, V>(B, ring + Cfg::RING, V ? vring + Cfg::RING : nullptr, bars_b, policy);
-            // C[kdone, kdone + teff) <- stage.  u = misc + k; stage slot = u - (u0 & ~3).
-            const int64_t cu0 = misc + kdone, cu1 = cu0 + teff;
-            const int64_t g0 = cu0 & ~int64_t(3);
-            const int64_t bs = (cu0 + 3) & ~int64_t(3);
-            const int64_t be = cu1 & ~int64_t(3);
-            int64_t p1 = cu1, q0 = cu1;
-            if (be > bs) {
-                bulk_copy_s2g(cbase16 + 4 * bs, stage_k + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
-                if (V) bulk_copy_s2g(cvbase16 + 4 * bs, stage_v + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
-                p1 = bs;
-                q0 = be;
+            S.head += side_a ? a_used : teff - a_used;
+            refill<Cfg, K, V>(S, rk, rv, bars, policy);
+            if (side_a) {
+                // C[kdone, kdone + teff) <- stage.  u = misc + k; stage slot = u - (u0 & ~3).
+                const int64_t cu0 = misc + kdone, cu1 = cu0 + teff;
+                const int64_t g0 = cu0 & ~int64_t(3);
+                const int64_t bs = (cu0 + 3) & ~int64_t(3);
+                const int64_t be = cu1 & ~int64_t(3);
+                int64_t p1 = cu1, q0 = cu1;
+                if (be > bs) {
+                    bulk_copy_s2g(cbase16 + 4 * bs, stage_k + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
+                    if (V) bulk_copy_s2g(cvbase16 + 4 * bs, stage_v + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
+                    p1 = bs;
+                    q0 = be;
+                }
+                K* ck = reinterpret_cast<K*>(cbase16);
+                uint32_t* cv = reinterpret_cast<uint32_t*>(cvbase16);
+                for (int64_t u = cu0; u < p1; ++u) {
+                    ck[u] = stage_k[u - g0];
+                    if (V) cv[u] = stage_v[u - g0];
+                }
+                for (int64_t u = q0; u < cu1; ++u) {
+                    ck[u] = stage_k[u - g0];
+                    if (V) cv[u] = stage_v[u - g0];
+                }
+                bulk_commit();
             }
-            K* ck = reinterpret_cast<K*>(cbase16);
-            uint32_t* cv = reinterpret_cast<uint32_t*>(cvbase16);
-            for (int64_t u = cu0; u < p1; ++u) {
-                ck[u] = stage_k[u - g0];
-                if (V) cv[u] = stage_v[u - g0];
-            }
-            for (int64_t u = q0; u < cu1; ++u) {
-                ck[u] = stage_k[u - g0];
-                if (V) cv[u] = stage_v[u - g0];
-            }
-            bulk_commit();
             kdone += teff;
         }
         if (failed) {
             // Let every requested chunk land (bounded) before the CTA's shared
             // memory is released; only the last NCH requests can be pending.
-            for (int side = 0; side < 2; ++side) {
-                SideStream* sp = side == 0 ? &A : &B;
-                uint64_t* bars = side == 0 ? bars_a : bars_b;
-                const int64_t c0 = sp->next_issue - Cfg::NCH > sp->c_first ? sp->next_issue - Cfg::NCH : sp->c_first;
-                for (int64_t c = c0; c < sp->next_issue; ++c) {
-                    const int rel = (int)(c - sp->c_first);
-                    mbar_wait_bounded(&bars[rel & (Cfg::NCH - 1)], (uint32_t)(rel >> Cfg::NCH_LOG2) & 1u, err);
-                }
+            const int64_t c0 = S.next_issue - Cfg::NCH > S.c_first ? S.next_issue - Cfg::NCH : S.c_first;
+            for (int64_t c = c0; c < S.next_issue; ++c) {
+                const int rel = (int)(c - S.c_first);
+                mbar_wait_bounded(&bars[rel & (Cfg::NCH - 1)], (uint32_t)(rel >> Cfg::NCH_LOG2) & 1u, err);
             }
         }
-        bulk_wait_all();
+        if (side_a) bulk_wait_all();
         return;
     }
 
