@@ -408,6 +408,10 @@ __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, 
     return ai - ha;
 }
 
+// A producer publishes a window cut to the data that has already landed when
+// the previous sub-tile's use of its side plus this margin fits in it.
+constexpr int kPartialMargin = 128;
+
 // Shared memory of the tile-merge kernel: keys of both rings back to back
 // (A ring, then B ring, so one masked index addresses either), values
 // likewise, the output stage, the chunk barriers of both sides, the
@@ -419,7 +423,9 @@ struct TileSmem {
     // chunk barriers of A and B, ready[2], done[2], stage_free
     static constexpr size_t bar_bytes = (size_t)(2 * Cfg::NCH + 5) * 8;
     // window descriptors: 2 x {ha, hb, wa, wb, teff, pad...} ints, a_used[2], abort
-    static constexpr size_t info_bytes = 2 * 8 * 4 + 4 * 4;
+    // window descriptors: 2 x {ha, hb, wa, wb, teff, partial_a, partial_b, -},
+    // a_used[2], redo[2], abort, padding
+    static constexpr size_t info_bytes = 2 * 8 * 4 + 8 * 4;
     static constexpr size_t total = ring_bytes + stage_bytes + bar_bytes + info_bytes;
 };
 
@@ -455,9 +461,10 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
     uint64_t* ready = bars_b + Cfg::NCH;  // [2]
     uint64_t* done = ready + 2;          // [2]
     uint64_t* stage_free = done + 2;     // [1]
-    int* info = reinterpret_cast<int*>(stage_free + 1);  // [2][8]: ha, hb, wa, wb, teff
+    int* info = reinterpret_cast<int*>(stage_free + 1);  // [2][8]: ha, hb, wa, wb, teff, partial a/b
     int* a_used_slot = info + 16;                        // [2]
-    volatile int* abort_flag = info + 18;
+    int* redo_slot = info + 18;                          // [2]
+    volatile int* abort_flag = info + 20;
 
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
@@ -475,7 +482,6 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         if (tid == 0) atomicOr(err, kErrBadRange);
         return;  // whole CTA
     }
-    const int nsub = (int)((k1 - k0 + T - 1) / T);
     const uintptr_t caddr = reinterpret_cast<uintptr_t>(s.ck);
     const int misc = (int)((caddr >> 2) & 3);
 
@@ -486,8 +492,8 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         }
         mbar_init(&ready[0], 2);  // both producers
         mbar_init(&ready[1], 2);
-        mbar_init(&done[0], NT);
-        mbar_init(&done[1], NT);
+        mbar_init(&done[0], NT + 1);  // consumers and the A producer
+        mbar_init(&done[1], NT + 1);
         mbar_init(stage_free, 1);
         fence_barrier_init();
         *abort_flag = 0;
@@ -516,27 +522,75 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         refill<Cfg, K, V>(S, rk, rv, bars, policy);
         int64_t kdone = k0;
         bool failed = false;
-        for (int it = 0; it < nsub; ++it) {
+        int64_t first_new = S.c_first;  // chunks from here on were requested by the latest refill
+        int last_used = -1;             // this side's consumption in the previous sub-tile
+        bool force_full = true;         // wait for the whole window (first sub-tile, after a redo)
+        for (int it = 0;; ++it) {
             const int teff = (int)((k1 - kdone) < T ? (k1 - kdone) : T);
-            const int w = (int)((S.u_hi - S.head) < T ? (S.u_hi - S.head) : T);
-            const bool ok = wait_window<Cfg>(S, S.head + w, bars, err);
             int* inf = info + 8 * (it & 1);
+            if (teff == 0) {  // every sub-tile is merged: tell the consumers to stop
+                if (side_a) inf[4] = 0;
+                mbar_arrive(&ready[it & 1]);
+                break;
+            }
+            const int need = (int)((S.u_hi - S.head) < T ? (S.u_hi - S.head) : T);
+            // Part of the window requested before the latest refill (landed by
+            // now); enough when last sub-tile's use of this side, plus a
+            // margin, fits in it.  Publishing it spares the consumers the
+            // DRAM latency of the chunks just requested.
+            const int64_t old_end = (first_new << Cfg::CH_LOG2) < S.u_hi ? (first_new << Cfg::CH_LOG2) : S.u_hi;
+            const int landed = (int)(old_end - S.head < need ? old_end - S.head : need);
+            int w = need;
+            int partial = 0;
+            if (!force_full && teff == T && landed < need && last_used >= 0 &&
+                last_used + kPartialMargin <= landed) {
+                w = landed;
+                partial = 1;
+            }
+            const bool ok = wait_window<Cfg>(S, S.head + w, bars, err);
             inf[side_a ? 0 : 1] = (int)((uint32_t)S.head & Cfg::RMASK);
             inf[side_a ? 2 : 3] = w;
+            inf[side_a ? 5 : 6] = partial;
             if (side_a) inf[4] = teff;
             if (!ok) *abort_flag = 1;
             mbar_arrive(&ready[it & 1]);  // release: this side's window and descriptor
-            if (side_a && it > 0) {
-                bulk_wait_read_all();  // the previous sub-tile's store has read the stage
-                mbar_arrive(stage_free);
+            if (side_a) {
+                if (it > 0) {
+                    bulk_wait_read_all();  // the previous sub-tile's store has read the stage
+                    mbar_arrive(stage_free);
+                }
+                // With both windows published, decide whether a cut window
+                // gives an exact sub-tile: its co-rank r on the windows must
+                // have r < wa and T - r < wb, so that every output's two heads
+                // lie inside them (r is then the true co-rank).  Runs while
+                // the consumers merge.
+                int redo = 0;
+                bool ok2 = mbar_wait_bounded(&ready[it & 1], (uint32_t)(it >> 1) & 1u, err);
+                if (ok2 && (inf[5] | inf[6])) {
+                    const int wa_ = inf[2], wb_ = inf[3];
+                    const int r = corank_ring<Cfg, K>(teff, teff - wb_ > 0 ? teff - wb_ : 0, teff < wa_ ? teff : wa_,
+                                                      ring, (uint32_t)inf[0], (uint32_t)inf[1]);
+                    a_used_slot[it & 1] = r;
+                    redo = (r < wa_ && teff - r < wb_) ? 0 : 1;
+                }
+                redo_slot[it & 1] = redo;
+                if (!ok2) *abort_flag = 1;
+                mbar_arrive(&done[it & 1]);  // release: a_used (cut windows) and redo flag
             }
             if (!ok || !mbar_wait_bounded(&done[it & 1], (uint32_t)(it >> 1) & 1u, err)) {
                 *abort_flag = 1;
                 failed = true;
                 break;
             }
+            if (redo_slot[it & 1]) {
+                force_full = true;  // same sub-tile again, with whole windows; nothing stored
+                continue;
+            }
+            force_full = false;
             const int a_used = a_used_slot[it & 1];
-            S.head += side_a ? a_used : teff - a_used;
+            last_used = side_a ? a_used : teff - a_used;
+            S.head += last_used;
+            first_new = S.next_issue;
             refill<Cfg, K, V>(S, rk, rv, bars, policy);
             if (side_a) {
                 // C[kdone, kdone + teff) <- stage.  u = misc + k; stage slot = u - (u0 & ~3).
@@ -580,17 +634,19 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
 
     // -------------------------------------------------------- consumers --
     const int dthr = tid * VT;
-    for (int it = 0; it < nsub; ++it) {
+    for (int it = 0;; ++it) {
         if (!mbar_wait_bounded(&ready[it & 1], (uint32_t)(it >> 1) & 1u, err) || *abort_flag) {
             *abort_flag = 1;
             return;
         }
         const int* inf = info + 8 * (it & 1);
+        const int teff = inf[4];
+        if (teff == 0) return;  // the producers have published the last sub-tile
         const uint32_t ha = (uint32_t)inf[0];
         const uint32_t hb = (uint32_t)inf[1];
         const int wa = inf[2];
         const int wb = inf[3];
-        const int teff = inf[4];
+        const bool partial = (inf[5] | inf[6]) != 0;
         const int d = dthr < teff ? dthr : teff;
         K keys[VT];
         uint32_t vals[VT];
@@ -599,6 +655,15 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         uint32_t apos;
         if (full) {
             const int a = corank_ring<Cfg, K>(d, 0, d, ring, ha, hb);
+            apos = merge_serial<Cfg, K, V, false>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
+        } else if (partial) {
+            // Windows cut to the data that has landed (teff == T).  Searches
+            // stay inside them and the merge runs without exhaustion tests;
+            // the A producer checks that the result is exact and, if not,
+            // the sub-tile is discarded and published again with whole windows.
+            const int lo = d - wb > 0 ? d - wb : 0;
+            const int hi = d < wa ? d : wa;
+            const int a = corank_ring<Cfg, K>(d, lo, hi, ring, ha, hb);
             apos = merge_serial<Cfg, K, V, false>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
         } else {
             cnt = (teff - d < VT) ? teff - d : VT;
@@ -611,7 +676,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
             *abort_flag = 1;
             return;
         }
-        if (full) {
+        if (cnt == VT) {
 #pragma unroll
             for (int v = 0; v < VT; ++v) {
                 stage_k[misc + d + v] = keys[v];
@@ -627,8 +692,8 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
             }
         }
         fence_proxy_async_smem();  // stage writes -> visible to the bulk store
-        if (tid == NT - 1) a_used_slot[it & 1] = (int)apos;  // = co_rank(teff)
-        mbar_arrive(&done[it & 1]);                          // release: stage, a_used, ring reads done
+        if (tid == NT - 1 && !partial) a_used_slot[it & 1] = (int)apos;  // = co_rank(teff)
+        mbar_arrive(&done[it & 1]);  // release: stage, a_used, ring reads done
     }
 }
 

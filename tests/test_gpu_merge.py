@@ -138,3 +138,37 @@ def test_merge_on_side_stream(gpu):
 
 def test_device_error_word_clear(gpu):
     assert gpu.device_error() == 0
+
+
+def _bursty(rng, nblocks, ties):
+    """Labels of a merged sequence: balanced stretches (A and B interleaved)
+    broken by long one-sided runs, so consecutive sub-tiles of one range use
+    each side very unevenly; values nondecreasing (with ties if asked)."""
+    labels = []
+    for q in range(nblocks):
+        kind = q % 7
+        if kind == 3:
+            labels += [0] * int(rng.integers(3000, 9000))      # A only
+        elif kind == 5:
+            labels += [1] * int(rng.integers(3000, 9000))      # B only
+        else:
+            labels += list(rng.integers(0, 2, int(rng.integers(2000, 6000))))
+    labels = np.array(labels)
+    vals = np.arange(labels.size, dtype=np.int64)
+    if ties:
+        vals //= 3
+    vals = (vals - labels.size // 2).astype(np.int32)
+    return vals[labels == 0], vals[labels == 1]
+
+
+@pytest.mark.parametrize("per_range", [8, 40])
+@pytest.mark.parametrize("ties", [False, True])
+def test_long_ranges_uneven_consumption(gpu, monkeypatch, per_range, ties):
+    """Many sub-tiles per output range with abrupt changes in how much each
+    sub-tile takes from A and B: exercises windows published before all of
+    their data was requested, and sub-tiles merged again with whole windows."""
+    monkeypatch.setenv("OM_SUBTILES_PER_RANGE", str(per_range))
+    rng = np.random.default_rng(per_range + 7 * ties)
+    A, B = _bursty(rng, 400, ties)
+    check(gpu, A, B)
+    check(gpu, B, A)

@@ -121,3 +121,21 @@ def test_sort_keys_only(gpu):
 def test_sort_workload_scaled(gpu):
     d = synth.make_host("sort", scale_log2=6)
     check_sort(gpu, d["keys"])
+
+
+@pytest.mark.parametrize("per_range", [8, 40])
+def test_pairs_long_ranges_uneven_consumption(gpu, monkeypatch, per_range):
+    """Key+value merge with many sub-tiles per range and bursty consumption."""
+    monkeypatch.setenv("OM_SUBTILES_PER_RANGE", str(per_range))
+    rng = np.random.default_rng(per_range)
+    labels = []
+    for q in range(300):
+        if q % 5 == 2:
+            labels += [q % 2] * int(rng.integers(2000, 6000))
+        else:
+            labels += list(rng.integers(0, 2, int(rng.integers(1000, 4000))))
+    labels = np.array(labels)
+    keys = (np.arange(labels.size) // 4).astype(np.uint32)
+    ka, kb = keys[labels == 0], keys[labels == 1]
+    va, vb = tagged(ka.size, kb.size)
+    check_pairs(gpu, ka, va, kb, vb)
