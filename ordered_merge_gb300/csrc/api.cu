@@ -36,12 +36,14 @@ template <>
 struct CfgFor<true> {
     using type = PairsCfg;
 };
-//  sort: runs of 1024 from a 128 x 8 block sort; early passes merge whole
-//        pairs of runs inside 256 x 16 = 4096-element tiles; later passes use
+//  sort: runs of 1024 from a 128 x 8 block sort; one early pass merges whole
+//        pairs of runs inside 256 x 16 = 4096-element tiles (1024 -> 4096);
+//        later passes use
 //        the partition + tile-merge kernels on each pair of runs.
 using RunSortCfg = BlockSortCfg<128, 8>;
 using SmallMergeCfg = BlockSortCfg<256, 16>;
-constexpr int kRunLen = RunSortCfg::TILE;  // 1024
+constexpr int kRunLen = RunSortCfg::TILE;     // 1024
+constexpr int kEarlyTo = SmallMergeCfg::TILE;  // 4096
 
 enum KernelKind { kKindPartition = 0, kKindTileMerge = 1, kKindBlockSort = 2, kKindCorank = 3, kNumKinds = 4 };
 
@@ -257,9 +259,13 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
     om_status s = device_state(&d);
     if (s != OM_OK) return s;
 
-    // Pass schedule.  Run sort to kRunLen, then one pass per doubling.
-    int passes = 0;
-    for (int64_t r = kRunLen; r < n; r *= 2) ++passes;
+    // Pass schedule: run sort to kRunLen in shared memory; one early pass
+    // that merges runs kRunLen -> kEarlyTo inside each block (whole pairs of
+    // runs per CTA, two merge steps in shared memory); then one co-rank-split
+    // late pass per doubling.  `passes` counts the global passes after the
+    // run sort.
+    int passes = n > kRunLen ? 1 : 0;
+    for (int64_t r = kEarlyTo; r < n; r *= 2) ++passes;
     using Cfg = typename CfgFor<V>::type;
     const int64_t subtiles = (n + Cfg::T - 1) / Cfg::T;
     const int64_t resident = (int64_t)d->sm_count * (V ? d->resident_merge_v : d->resident_merge);
@@ -267,8 +273,7 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
     // splitter slots for the largest late pass (every pair gets the same
     // number of ranges, including a short last pair), plus one
     int64_t max_ranges = 1;
-    for (int64_t r = kRunLen; r < n; r *= 2) {
-        if (2 * r <= SmallMergeCfg::TILE) continue;
+    for (int64_t r = kEarlyTo; r < n; r *= 2) {
         const int64_t npairs = (n + 2 * r - 1) / (2 * r);
         const int64_t rps = (2 * r + range_len - 1) / range_len;
         if (npairs * rps + 1 > max_ranges) max_ranges = npairs * rps + 1;
@@ -303,27 +308,28 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
                 keys, vals, src_k, src_v, n, 1, kRunLen);
         });
     }
-    for (int64_t r = kRunLen; e == cudaSuccess && r < n; r *= 2) {
-        if (2 * r <= SmallMergeCfg::TILE) {
-            // early pass: each CTA merges whole pairs of runs inside its tile
-            const unsigned grid = (unsigned)((n + SmallMergeCfg::TILE - 1) / SmallMergeCfg::TILE);
-            e = traced(kKindBlockSort, st, [&] {
-                block_sort_kernel<SmallMergeCfg, V>
-                    <<<grid, SmallMergeCfg::NT, block_sort_smem_bytes<SmallMergeCfg, V>(), st>>>(
-                        src_k, src_v, dst_k, dst_v, n, (int)r, (int)(2 * r));
-            });
-        } else {
-            // late pass: co-rank split of each pair of runs into output ranges
-            const int64_t npairs = (n + 2 * r - 1) / (2 * r);
-            const int64_t rps = (2 * r + range_len - 1) / range_len;
-            MergeGeom<uint32_t> g{src_k, src_v, nullptr, nullptr, dst_k, dst_v, n, 0, r, range_len, rps,
-                                  npairs * rps};
-            if (g.nranges + 1 > max_ranges || g.nranges > 0x7fffffff) {
-                e = cudaErrorInvalidValue;
-                break;
-            }
-            e = launch_merge<uint32_t, V>(g, split, d, st);
+    if (e == cudaSuccess && n > kRunLen) {
+        // early pass: each CTA merges whole pairs of runs inside its tile,
+        // kRunLen -> kEarlyTo
+        const unsigned grid = (unsigned)((n + SmallMergeCfg::TILE - 1) / SmallMergeCfg::TILE);
+        e = traced(kKindBlockSort, st, [&] {
+            block_sort_kernel<SmallMergeCfg, V><<<grid, SmallMergeCfg::NT, block_sort_smem_bytes<SmallMergeCfg, V>(),
+                                                  st>>>(src_k, src_v, dst_k, dst_v, n, kRunLen, kEarlyTo);
+        });
+        uint32_t* t;
+        t = src_k; src_k = dst_k; dst_k = t;
+        t = src_v; src_v = dst_v; dst_v = t;
+    }
+    for (int64_t r = kEarlyTo; e == cudaSuccess && r < n; r *= 2) {
+        // late pass: co-rank split of each pair of runs into output ranges
+        const int64_t npairs = (n + 2 * r - 1) / (2 * r);
+        const int64_t rps = (2 * r + range_len - 1) / range_len;
+        MergeGeom<uint32_t> g{src_k, src_v, nullptr, nullptr, dst_k, dst_v, n, 0, r, range_len, rps, npairs * rps};
+        if (g.nranges + 1 > max_ranges || g.nranges > 0x7fffffff) {
+            e = cudaErrorInvalidValue;
+            break;
         }
+        e = launch_merge<uint32_t, V>(g, split, d, st);
         uint32_t* t;
         t = src_k; src_k = dst_k; dst_k = t;
         t = src_v; src_v = dst_v; dst_v = t;

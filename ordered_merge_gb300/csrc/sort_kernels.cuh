@@ -49,17 +49,17 @@ constexpr size_t block_sort_smem_bytes() {
     return (size_t)Cfg::PADDED * 4 * (V ? 2 : 1);
 }
 
-// co_rank(d) of A = s[pad(a0 + x)], x < m and B = s[pad(b0 + x)], x < n.
-__device__ __forceinline__ int corank_padded(int d, const uint32_t* s, int a0, int m, int b0, int n) {
+// co_rank(d) of A = s[pad(a0 + x)], x < m and B = s[pad(b0 + x)], x < n:
+// the largest i in [max(0,d-n), min(d,m)] with i at the lower bound or
+// A[i-1] <= B[d-i], by power-of-two steps from `top` (a power of two with
+// 2 * top > min(d,m) - max(0,d-n)), so every thread of a pass takes the same
+// number of steps.
+__device__ __forceinline__ int corank_padded(int d, const uint32_t* s, int a0, int m, int b0, int n, int top) {
     int lo = d - n > 0 ? d - n : 0;
-    int hi = d < m ? d : m;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s[pad32(a0 + mid - 1)] <= s[pad32(b0 + d - mid)]) {
-            lo = mid;
-        } else {
-            hi = mid - 1;
-        }
+    const int hi = d < m ? d : m;
+    for (int step = top; step > 0; step >>= 1) {
+        const int cand = lo + step;
+        if (cand <= hi && s[pad32(a0 + cand - 1)] <= s[pad32(b0 + d - cand)]) lo = cand;
     }
     return lo;
 }
@@ -136,24 +136,35 @@ __global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const uint32_t* in_
             const int nb = nb_raw <= 0 ? 0 : (nb_raw < w ? nb_raw : w);
             const int b0 = a0 + w;
             cnt = (m + nb - d) < VT ? (m + nb - d) : VT;
-            int a = corank_padded(d, sk, a0, m, b0, nb);
-            int b = d - a;
-            uint32_t ak = (a < m) ? sk[pad32(a0 + a)] : 0u;
-            uint32_t bk = (b < nb) ? sk[pad32(b0 + b)] : 0u;
+            const int a = corank_padded(d, sk, a0, m, b0, nb, w);
+            // Serial merge with selects: A and B are adjacent runs, so one
+            // index (clamped into the tile) reaches either head.  Take A
+            // unless A is exhausted or B's head is strictly smaller.
+            int ia = a0 + a, ib = b0 + (d - a);
+            const int ea = a0 + m, eb = b0 + nb;
+            int x = ia < TILE - 1 ? ia : TILE - 1;
+            int y = ib < TILE - 1 ? ib : TILE - 1;
+            uint32_t ak = sk[pad32(x)], bk = sk[pad32(y)];
+            uint32_t av = V ? sv[pad32(x)] : 0u, bv = V ? sv[pad32(y)] : 0u;
 #pragma unroll
             for (int i = 0; i < VT; ++i) {
                 if (i < cnt) {
-                    const bool take_a = (b >= nb) || (a < m && ak <= bk);
-                    if (take_a) {
-                        k[i] = ak;
-                        if (V) v[i] = sv[pad32(a0 + a)];
-                        ++a;
-                        if (a < m) ak = sk[pad32(a0 + a)];
-                    } else {
-                        k[i] = bk;
-                        if (V) v[i] = sv[pad32(b0 + b)];
-                        ++b;
-                        if (b < nb) bk = sk[pad32(b0 + b)];
+                    const bool p = (ib >= eb) || (ia < ea && ak <= bk);
+                    k[i] = p ? ak : bk;
+                    if (V) v[i] = p ? av : bv;
+                    ia += p ? 1 : 0;
+                    ib += p ? 0 : 1;
+                    if (i + 1 < VT) {
+                        int idx = p ? ia : ib;
+                        idx = idx < TILE - 1 ? idx : TILE - 1;
+                        const uint32_t nk = sk[pad32(idx)];
+                        ak = p ? nk : ak;
+                        bk = p ? bk : nk;
+                        if (V) {
+                            const uint32_t nv = sv[pad32(idx)];
+                            av = p ? nv : av;
+                            bv = p ? bv : nv;
+                        }
                     }
                 }
             }
