@@ -96,10 +96,11 @@ om_status om_merge_pairs_u32(const uint32_t *keysA, const uint32_t *valsA,
 
 /*
  * Stable sort of keys[0..n) (unsigned order), in place, carrying vals along
- * (vals may be NULL for a keys-only sort).  Built only from merges: runs of
- * 1024 are sorted in shared memory, then runs are merged pairwise, with many
- * small merges per thread block in early passes and co-rank-split large
- * merges in late passes ("排序 (Sorting) 練習題", merge-sort stages).
+ * (vals may be NULL for a keys-only sort).  Built only from merges: tiles of
+ * 4096 are sorted in shared memory (runs of 16 in registers, then many small
+ * merges per thread block through runs of 1024 to 4096), then runs are
+ * merged pairwise in co-rank-split passes ("排序 (Sorting) 練習題",
+ * merge-sort stages).
  * Equal keys keep their input order.  Needs 4*n (8*n with vals) bytes of
  * stream-ordered scratch.
  */

@@ -36,14 +36,12 @@ template <>
 struct CfgFor<true> {
     using type = PairsCfg;
 };
-//  sort: runs of 1024 from a 128 x 8 block sort; one early pass merges whole
-//        pairs of runs inside 256 x 16 = 4096-element tiles (1024 -> 4096);
-//        later passes use
+//  sort: one block pass sorts 256 x 16 = 4096-element tiles in shared memory
+//        (runs of 16 in registers, then merges of whole pairs of runs per
+//        CTA through 1024 to 4096); later passes use
 //        the partition + tile-merge kernels on each pair of runs.
-using RunSortCfg = BlockSortCfg<128, 8>;
 using SmallMergeCfg = BlockSortCfg<256, 16>;
-constexpr int kRunLen = RunSortCfg::TILE;     // 1024
-constexpr int kEarlyTo = SmallMergeCfg::TILE;  // 4096
+constexpr int kEarlyTo = SmallMergeCfg::TILE;  // runs after the block pass: 4096
 
 enum KernelKind { kKindPartition = 0, kKindTileMerge = 1, kKindBlockSort = 2, kKindCorank = 3, kNumKinds = 4 };
 
@@ -88,8 +86,6 @@ static om_status device_state(DeviceState** out) {
         e = e ? e : set_smem(tile_merge_kernel<MergeCfg, int32_t, false>, TileSmem<MergeCfg, false>::total);
         e = e ? e : set_smem(tile_merge_kernel<MergeCfg, uint32_t, false>, TileSmem<MergeCfg, false>::total);
         e = e ? e : set_smem(tile_merge_kernel<PairsCfg, uint32_t, true>, TileSmem<PairsCfg, true>::total);
-        e = e ? e : set_smem(block_sort_kernel<RunSortCfg, true>, block_sort_smem_bytes<RunSortCfg, true>());
-        e = e ? e : set_smem(block_sort_kernel<RunSortCfg, false>, block_sort_smem_bytes<RunSortCfg, false>());
         e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, true>, block_sort_smem_bytes<SmallMergeCfg, true>());
         e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, false>, block_sort_smem_bytes<SmallMergeCfg, false>());
         if (e != cudaSuccess) return OM_ECUDA;
@@ -259,12 +255,11 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
     om_status s = device_state(&d);
     if (s != OM_OK) return s;
 
-    // Pass schedule: run sort to kRunLen in shared memory; one early pass
-    // that merges runs kRunLen -> kEarlyTo inside each block (whole pairs of
-    // runs per CTA, two merge steps in shared memory); then one co-rank-split
-    // late pass per doubling.  `passes` counts the global passes after the
-    // run sort.
-    int passes = n > kRunLen ? 1 : 0;
+    // Pass schedule: one block pass sorts each 4096-element tile in shared
+    // memory (early stages: many small merges per block); then one
+    // co-rank-split late pass per doubling.  `passes` counts the global
+    // passes after the block pass.
+    int passes = 0;
     for (int64_t r = kEarlyTo; r < n; r *= 2) ++passes;
     using Cfg = typename CfgFor<V>::type;
     const int64_t subtiles = (n + Cfg::T - 1) / Cfg::T;
@@ -294,31 +289,22 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
             return OM_ENOMEM;
         }
     }
-    // The run sort writes where the pass count's parity makes the last pass
-    // land back in keys / vals.
+    // The block pass writes where the pass count's parity makes the last
+    // pass land back in keys / vals.
     uint32_t* src_k = (passes % 2 == 0) ? keys : tk;
     uint32_t* src_v = (passes % 2 == 0) ? vals : tv;
     uint32_t* dst_k = (passes % 2 == 0) ? tk : keys;
     uint32_t* dst_v = (passes % 2 == 0) ? tv : vals;
 
     {
-        const unsigned grid = (unsigned)((n + RunSortCfg::TILE - 1) / RunSortCfg::TILE);
-        e = traced(kKindBlockSort, st, [&] {
-            block_sort_kernel<RunSortCfg, V><<<grid, RunSortCfg::NT, block_sort_smem_bytes<RunSortCfg, V>(), st>>>(
-                keys, vals, src_k, src_v, n, 1, kRunLen);
-        });
-    }
-    if (e == cudaSuccess && n > kRunLen) {
-        // early pass: each CTA merges whole pairs of runs inside its tile,
-        // kRunLen -> kEarlyTo
+        // run sort and early merges in one launch: every CTA sorts 16
+        // elements per thread in registers, then merges runs 16 -> ... ->
+        // 1024 -> ... -> kEarlyTo in shared memory (whole pairs per CTA)
         const unsigned grid = (unsigned)((n + SmallMergeCfg::TILE - 1) / SmallMergeCfg::TILE);
         e = traced(kKindBlockSort, st, [&] {
             block_sort_kernel<SmallMergeCfg, V><<<grid, SmallMergeCfg::NT, block_sort_smem_bytes<SmallMergeCfg, V>(),
-                                                  st>>>(src_k, src_v, dst_k, dst_v, n, kRunLen, kEarlyTo);
+                                                  st>>>(keys, vals, src_k, src_v, n, 1, kEarlyTo);
         });
-        uint32_t* t;
-        t = src_k; src_k = dst_k; dst_k = t;
-        t = src_v; src_v = dst_v; dst_v = t;
     }
     for (int64_t r = kEarlyTo; e == cudaSuccess && r < n; r *= 2) {
         // late pass: co-rank split of each pair of runs into output ranges
