@@ -25,9 +25,9 @@ namespace om {
 //         dominates, so the largest sub-tile and chunk that fit a 4096 ring win.)
 using MergeCfg = TileCfg<128, 23, 12, 10>;
 //  key+value merge: four rings (keys and values of A and B), so smaller rings
-//  keep 5 CTAs per SM: 96 x 15 = 1440 outputs per sub-tile, 2048-element
-//  rings, 512-element chunks (best of eight shapes measured on GB300).
-using PairsCfg = TileCfg<96, 15, 11, 9>;
+//  keep 5 CTAs per SM: 128 x 11 = 1408 outputs per sub-tile, 2048-element
+//  rings, 512-element chunks (best of the shapes measured on GB300).
+using PairsCfg = TileCfg<128, 11, 11, 9>;
 template <bool V>
 struct CfgFor {
     using type = MergeCfg;
