@@ -8,7 +8,8 @@ here with gcc and called through ctypes on numpy arrays.
 
 Functions (see ``merge_oracle.c`` for the definition each one restates):
 
-* :func:`merge_i32`, :func:`merge_pairs_u32` -- two-pointer stable merge (O1)
+* :func:`merge_i32`, :func:`merge_u32`, :func:`merge_f32`,
+  :func:`merge_pairs_u32` -- two-pointer stable merge (O1)
 * :func:`corank_pages` -- the pages' co-rank bisection, with trace (O2)
 * :func:`corank_count` -- co-rank by counting merge steps (O3)
 * :func:`merge_sort_pairs_u32` -- bottom-up stable merge sort from O1 (O4)
@@ -70,6 +71,10 @@ def load(path: str | None = None):
 def _declare(lib):
     lib.oracle_merge_i32.argtypes = [_P, _I64, _P, _I64, _P]
     lib.oracle_merge_i32.restype = None
+    lib.oracle_merge_u32.argtypes = [_P, _I64, _P, _I64, _P]
+    lib.oracle_merge_u32.restype = None
+    lib.oracle_merge_f32.argtypes = [_P, _I64, _P, _I64, _P]
+    lib.oracle_merge_f32.restype = None
     lib.oracle_merge_pairs_u32.argtypes = [_P, _P, _I64, _P, _P, _I64, _P, _P]
     lib.oracle_merge_pairs_u32.restype = None
     lib.oracle_corank_pages_i32.argtypes = [_I64, _P, _I64, _P, _I64, _P, _I64, _P]
@@ -101,6 +106,26 @@ def merge_i32(A, B, lib=None) -> np.ndarray:
     B = _arr(B, np.int32)
     C = np.empty(A.size + B.size, dtype=np.int32)
     lib.oracle_merge_i32(_ptr(A), A.size, _ptr(B), B.size, _ptr(C))
+    return C
+
+
+def merge_u32(A, B, lib=None) -> np.ndarray:
+    """O1 on uint32 keys (unsigned order)."""
+    lib = lib or load()
+    A = _arr(A, np.uint32)
+    B = _arr(B, np.uint32)
+    C = np.empty(A.size + B.size, dtype=np.uint32)
+    lib.oracle_merge_u32(_ptr(A), A.size, _ptr(B), B.size, _ptr(C))
+    return C
+
+
+def merge_f32(A, B, lib=None) -> np.ndarray:
+    """O1 on float32 keys (float order; keys comparing equal keep A first)."""
+    lib = lib or load()
+    A = _arr(A, np.float32)
+    B = _arr(B, np.float32)
+    C = np.empty(A.size + B.size, dtype=np.float32)
+    lib.oracle_merge_f32(_ptr(A), A.size, _ptr(B), B.size, _ptr(C))
     return C
 
 

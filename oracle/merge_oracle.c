@@ -16,8 +16,8 @@
  *   [P4] "merge_path.cu"
  *
  * Contents
- *   O1  oracle_merge_i32 / oracle_merge_pairs_u32: the two-pointer stable
- *       merge.  Equal keys take A first.  ([P1] §Overview, acceptance row;
+ *   O1  oracle_merge_i32 / _u32 / _f32 / oracle_merge_pairs_u32: the
+ *       two-pointer stable merge.  Equal keys take A first.  ([P1] §Overview, acceptance row;
  *       [P4] mergeCpu, "CPU reference".)
  *   O2  oracle_corank_pages_i32: the co-rank bisection in the order and
  *       notation of [P1] §Binary-Search Implementation (i, j, i_low, j_low,
@@ -58,6 +58,40 @@ void oracle_merge_i32(const int32_t *A, int64_t m, const int32_t *B,
             C[k++] = B[j++];
         } else {
             C[k++] = A[i++]; /* A[i] <= B[j]: A first, also on a tie */
+        }
+    }
+    while (i < m) C[k++] = A[i++];
+    while (j < n) C[k++] = B[j++];
+}
+
+/* O1 on uint32 keys (unsigned order). */
+void oracle_merge_u32(const uint32_t *A, int64_t m, const uint32_t *B,
+                      int64_t n, uint32_t *C)
+{
+    int64_t i = 0, j = 0, k = 0;
+    while (i < m && j < n) {
+        if (B[j] < A[i]) {
+            C[k++] = B[j++];
+        } else {
+            C[k++] = A[i++];
+        }
+    }
+    while (i < m) C[k++] = A[i++];
+    while (j < n) C[k++] = B[j++];
+}
+
+/* O1 on float keys with the float order of merge_path.cu's mergeCpu: B goes
+ * first only when B[j] < A[i] as floats, so keys that compare equal (for
+ * example -0.0 and +0.0) keep A first.  Inputs must not hold NaN. */
+void oracle_merge_f32(const float *A, int64_t m, const float *B, int64_t n,
+                      float *C)
+{
+    int64_t i = 0, j = 0, k = 0;
+    while (i < m && j < n) {
+        if (B[j] < A[i]) {
+            C[k++] = B[j++];
+        } else {
+            C[k++] = A[i++];
         }
     }
     while (i < m) C[k++] = A[i++];

@@ -24,6 +24,11 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "merge_oracle.c")
 # equivalent: no input can tell it apart.  An exhaustive search over all
 # sorted inputs of total length <= 8 on a 4-letter alphabet agreed.
 #
+# Not listed either: taking B first on a tie in the keys-only uint32 merge.
+# Equal uint32 keys are the same bits, so the output cannot show which side
+# went first; the float merge's tie rule is pinned instead, through -0.0 and
+# +0.0, which compare equal but differ in bits.
+#
 # (name, exact text in the oracle, replacement, occurrence index to replace)
 MUTANTS = [
     ("pairs_ties_take_B_first", "if (keysB[j] < keysA[i]) {", "if (keysB[j] <= keysA[i]) {", 0),
@@ -37,14 +42,21 @@ MUTANTS = [
     ("merge_at_B_first_on_tie", "int take_a = (i < m) && (j >= n || A[i] <= B[j]);", "int take_a = (i < m) && (j >= n || A[i] < B[j]);", 0),
     ("sort_later_run_first", "oracle_merge_pairs_u32(src_k + lo, src_v + lo, mid - lo,\n                                   src_k + mid, src_v + mid, hi - mid,",
      "oracle_merge_pairs_u32(src_k + mid, src_v + mid, hi - mid,\n                                   src_k + lo, src_v + lo, mid - lo,", 0),
+    ("u32_signed_compare", "void oracle_merge_u32(const uint32_t *A, int64_t m, const uint32_t *B,",
+     "void oracle_merge_u32(const int32_t *A, int64_t m, const int32_t *B,", 0),
+    ("f32_B_first_on_tie", "if (B[j] < A[i]) {", "if (B[j] <= A[i]) {", 2),
+    ("f32_drops_B_tail", "    while (j < n) C[k++] = B[j++];\n", "\n", 2),
     ("sort_stops_one_pass_early", "for (int64_t width = 1; width < n; width *= 2) {", "for (int64_t width = 2; width < n; width *= 2) {", 0),
 ]
 
 
-def _build_mutant(tmp_path, name, old, new):
+def _build_mutant(tmp_path, name, old, new, occ=0):
     src = open(SRC).read()
-    assert src.count(old) >= 1, f"mutation site for {name} not found in the oracle"
-    mutated = src.replace(old, new, 1)
+    assert src.count(old) > occ, f"mutation site for {name} not found in the oracle"
+    at = -1
+    for _ in range(occ + 1):
+        at = src.index(old, at + 1)
+    mutated = src[:at] + new + src[at + len(old):]
     c = tmp_path / f"{name}.c"
     so = tmp_path / f"lib{name}.so"
     c.write_text(mutated)
@@ -63,6 +75,8 @@ for check in ALL_CHECKS:
     try:
         if check.__name__ == "check_brute_force":
             check(lib, max_len=4)
+        elif check.__name__ == "check_typed_keys":
+            check(lib, max_len=3)
         else:
             check(lib)
     except Exception:
@@ -73,7 +87,7 @@ print("CAUGHT", ",".join(caught))
 
 @pytest.mark.parametrize("name,old,new,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_pins_catch_mutant(tmp_path, name, old, new, occ):
-    so = _build_mutant(tmp_path, name, old, new)
+    so = _build_mutant(tmp_path, name, old, new, occ)
     tests_dir = os.path.dirname(os.path.abspath(__file__))
     code = _RUNNER.format(root=os.path.dirname(tests_dir), tests=tests_dir, so=so)
     proc = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)

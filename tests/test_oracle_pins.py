@@ -214,6 +214,61 @@ def check_merge_sort(lib, seed=9):
         assert np.all(np.diff(sk.astype(np.int64)) >= 0)
 
 
+def _stable_merge_by(A, B, key):
+    """Python's stable sort of A's items then B's items; returns (value, side)."""
+    tagged = sorted([(a, 0) for a in A] + [(b, 1) for b in B], key=lambda t: key(t[0]))
+    return tagged
+
+
+def check_typed_keys(lib, max_len=4):
+    """O1 on uint32 and float32 keys.
+
+    uint32: every pair of sorted inputs over an alphabet that straddles the
+    sign bit equals the stable sort of the concatenation by unsigned value,
+    so a signed compare (0x80000000 before 0) fails.  float32: the alphabet
+    holds -inf, a negative, -0.0 and +0.0 (equal as floats, different bits),
+    a subnormal and +inf; the merge must equal the stable sort by float value
+    bit for bit, so comparing raw bits (negatives reversed) or taking B first
+    on a tie (+0.0 of B ahead of -0.0 of A) fails."""
+    u_alpha = (0, 1, 0x7FFFFFFF, 0x80000000, 0xFFFFFFFF)
+    seqs = [list(s) for s in _sorted_seqs(max_len, u_alpha)]
+    for A in seqs:
+        for B in seqs:
+            want = [v for v, _ in _stable_merge_by(A, B, key=int)]
+            got = oracle.merge_u32(np.array(A, np.uint32), np.array(B, np.uint32), lib=lib)
+            assert [int(x) for x in got] == want, (A, B)
+    f_alpha = np.array([-np.inf, -1.5, -0.0, 0.0, 1e-45, np.inf], dtype=np.float32)
+    # sorted by float order, -0.0 and +0.0 equal; every order of the two zeros
+    # inside a sequence is a valid sorted input, so enumerate bit patterns
+    bits = [int(x) for x in f_alpha.view(np.uint32)]
+    fval = {b: float(np.array([b], np.uint32).view(np.float32)[0]) for b in bits}
+    fseqs = []
+    for L in range(max_len + 1):
+        for combo in itertools.product(bits, repeat=L):
+            if all(fval[combo[t]] <= fval[combo[t + 1]] for t in range(L - 1)):
+                fseqs.append(list(combo))
+    rng = np.random.default_rng(17)
+    pick = rng.choice(len(fseqs), size=min(len(fseqs), 140), replace=False)
+    sub = [fseqs[int(t)] for t in pick] + [[], [bits[2]], [bits[3]]]
+    for A in sub:
+        for B in sub:
+            want = [v for v, _ in _stable_merge_by(A, B, key=lambda b: fval[b])]
+            got = oracle.merge_f32(np.array(A, np.uint32).view(np.float32),
+                                   np.array(B, np.uint32).view(np.float32), lib=lib)
+            assert [int(x) for x in got.view(np.uint32)] == want, (A, B)
+    # larger random inputs against numpy's stable argsort of the concatenation
+    for m, n in [(0, 7), (7, 0), (1000, 999), (4097, 33)]:
+        a = np.sort(rng.integers(0, 1 << 32, m, dtype=np.uint64)).astype(np.uint32)
+        b = np.sort(rng.integers(0, 1 << 32, n, dtype=np.uint64)).astype(np.uint32)
+        cat = np.concatenate([a, b])
+        assert np.array_equal(oracle.merge_u32(a, b, lib=lib), cat[np.argsort(cat, kind="stable")])
+        fa = np.sort(rng.choice(f_alpha, m).astype(np.float32) * rng.integers(1, 4, m).astype(np.float32))
+        fb = np.sort(rng.choice(f_alpha, n).astype(np.float32) * rng.integers(1, 4, n).astype(np.float32))
+        fcat = np.concatenate([fa, fb])
+        got = oracle.merge_f32(fa, fb, lib=lib)
+        assert np.array_equal(got.view(np.uint32), fcat[np.argsort(fcat, kind="stable")].view(np.uint32))
+
+
 ALL_CHECKS = [
     check_worked_example,
     check_tie_case,
@@ -222,6 +277,7 @@ ALL_CHECKS = [
     check_pairs_ties_closed_form,
     check_invariants_random,
     check_merge_sort,
+    check_typed_keys,
 ]
 
 
