@@ -8,7 +8,7 @@ here with gcc and called through ctypes on numpy arrays.
 
 Functions (see ``merge_oracle.c`` for the definition each one restates):
 
-* :func:`merge_i32`, :func:`merge_u32`, :func:`merge_f32`,
+* :func:`merge_i32`, :func:`merge_u32`, :func:`merge_f32`, :func:`merge_keys`,
   :func:`merge_pairs_u32` -- two-pointer stable merge (O1)
 * :func:`corank_pages` -- the pages' co-rank bisection, with trace (O2)
 * :func:`corank_count` -- co-rank by counting merge steps (O3)
@@ -75,6 +75,8 @@ def _declare(lib):
     lib.oracle_merge_u32.restype = None
     lib.oracle_merge_f32.argtypes = [_P, _I64, _P, _I64, _P]
     lib.oracle_merge_f32.restype = None
+    lib.oracle_merge_keys.argtypes = [ctypes.c_int, ctypes.c_int, _P, _I64, _P, _I64, _P]
+    lib.oracle_merge_keys.restype = ctypes.c_int
     lib.oracle_merge_pairs_u32.argtypes = [_P, _P, _I64, _P, _P, _I64, _P, _P]
     lib.oracle_merge_pairs_u32.restype = None
     lib.oracle_corank_pages_i32.argtypes = [_I64, _P, _I64, _P, _I64, _P, _I64, _P]
@@ -126,6 +128,26 @@ def merge_f32(A, B, lib=None) -> np.ndarray:
     B = _arr(B, np.float32)
     C = np.empty(A.size + B.size, dtype=np.float32)
     lib.oracle_merge_f32(_ptr(A), A.size, _ptr(B), B.size, _ptr(C))
+    return C
+
+
+# the oracle's key-type codes, by numpy dtype
+KEY_CODES = {np.dtype(np.int32): 0, np.dtype(np.uint32): 1, np.dtype(np.float32): 2,
+             np.dtype(np.int64): 3, np.dtype(np.uint64): 4, np.dtype(np.float64): 5}
+
+
+def merge_keys(A, B, descending=False, lib=None) -> np.ndarray:
+    """O1 for any of the six key types (taken from A's dtype), either order."""
+    lib = lib or load()
+    A = np.ascontiguousarray(A)
+    dt = A.dtype
+    if dt not in KEY_CODES:
+        raise ValueError(f"no oracle key type for {dt}")
+    B = _arr(B, dt)
+    C = np.empty(A.size + B.size, dtype=dt)
+    rc = lib.oracle_merge_keys(KEY_CODES[dt], 1 if descending else 0, _ptr(A), A.size, _ptr(B), B.size, _ptr(C))
+    if rc != 0:
+        raise ValueError("oracle_merge_keys rejected the key type")
     return C
 
 

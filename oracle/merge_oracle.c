@@ -16,8 +16,9 @@
  *   [P4] "merge_path.cu"
  *
  * Contents
- *   O1  oracle_merge_i32 / _u32 / _f32 / oracle_merge_pairs_u32: the
- *       two-pointer stable merge.  Equal keys take A first.  ([P1] §Overview, acceptance row;
+ *   O1  oracle_merge_i32 / _u32 / _f32 / oracle_merge_pairs_u32 /
+ *       oracle_merge_keys (six key types, either order): the two-pointer
+ *       stable merge.  Equal keys take A first.  ([P1] §Overview, acceptance row;
  *       [P4] mergeCpu, "CPU reference".)
  *   O2  oracle_corank_pages_i32: the co-rank bisection in the order and
  *       notation of [P1] §Binary-Search Implementation (i, j, i_low, j_low,
@@ -96,6 +97,89 @@ void oracle_merge_f32(const float *A, int64_t m, const float *B, int64_t n,
     }
     while (i < m) C[k++] = A[i++];
     while (j < n) C[k++] = B[j++];
+}
+
+/*
+ * O1 for keys of other types and for descending order.  `type` is one of the
+ * ORACLE_KEY_* codes below; desc = 0 merges nondecreasing inputs, desc = 1
+ * nonincreasing ones.  B's head goes out first only when it comes strictly
+ * before A's head in the order (ascending: B[j] < A[i]; descending:
+ * B[j] > A[i]), so equal keys keep A first in both orders.  Floats compare
+ * as IEEE values (-0.0 == +0.0); inputs must not hold NaN.  Returns 0, or
+ * -1 for an unknown type.
+ */
+enum {
+    ORACLE_KEY_I32 = 0,
+    ORACLE_KEY_U32 = 1,
+    ORACLE_KEY_F32 = 2,
+    ORACLE_KEY_I64 = 3,
+    ORACLE_KEY_U64 = 4,
+    ORACLE_KEY_F64 = 5
+};
+
+static size_t oracle_key_size(int type)
+{
+    switch (type) {
+    case ORACLE_KEY_I32: case ORACLE_KEY_U32: case ORACLE_KEY_F32: return 4;
+    case ORACLE_KEY_I64: case ORACLE_KEY_U64: case ORACLE_KEY_F64: return 8;
+    default: return 0;
+    }
+}
+
+/* 1 when B[j] comes strictly before A[i] in the merge order. */
+static int oracle_b_before_a(int type, int desc, const void *A, int64_t i,
+                             const void *B, int64_t j)
+{
+    switch (type) {
+    case ORACLE_KEY_I32: {
+        int32_t x = ((const int32_t *)A)[i], y = ((const int32_t *)B)[j];
+        return desc ? (y > x) : (y < x);
+    }
+    case ORACLE_KEY_U32: {
+        uint32_t x = ((const uint32_t *)A)[i], y = ((const uint32_t *)B)[j];
+        return desc ? (y > x) : (y < x);
+    }
+    case ORACLE_KEY_F32: {
+        float x = ((const float *)A)[i], y = ((const float *)B)[j];
+        return desc ? (y > x) : (y < x);
+    }
+    case ORACLE_KEY_I64: {
+        int64_t x = ((const int64_t *)A)[i], y = ((const int64_t *)B)[j];
+        return desc ? (y > x) : (y < x);
+    }
+    case ORACLE_KEY_U64: {
+        uint64_t x = ((const uint64_t *)A)[i], y = ((const uint64_t *)B)[j];
+        return desc ? (y > x) : (y < x);
+    }
+    default: {
+        double x = ((const double *)A)[i], y = ((const double *)B)[j];
+        return desc ? (y > x) : (y < x);
+    }
+    }
+}
+
+int oracle_merge_keys(int type, int desc, const void *A, int64_t m,
+                      const void *B, int64_t n, void *C)
+{
+    const size_t e = oracle_key_size(type);
+    const unsigned char *a = (const unsigned char *)A;
+    const unsigned char *b = (const unsigned char *)B;
+    unsigned char *c = (unsigned char *)C;
+    int64_t i = 0, j = 0, k = 0;
+    if (e == 0) return -1;
+    while (i < m && j < n) {
+        if (oracle_b_before_a(type, desc, A, i, B, j)) {
+            memcpy(c + (size_t)k * e, b + (size_t)j * e, e);
+            ++j;
+        } else {
+            memcpy(c + (size_t)k * e, a + (size_t)i * e, e);
+            ++i;
+        }
+        ++k;
+    }
+    for (; i < m; ++i, ++k) memcpy(c + (size_t)k * e, a + (size_t)i * e, e);
+    for (; j < n; ++j, ++k) memcpy(c + (size_t)k * e, b + (size_t)j * e, e);
+    return 0;
 }
 
 /* Same rule on unsigned keys; each value travels with its key. */

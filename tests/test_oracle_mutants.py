@@ -46,6 +46,16 @@ MUTANTS = [
      "void oracle_merge_u32(const int32_t *A, int64_t m, const int32_t *B,", 0),
     ("f32_B_first_on_tie", "if (B[j] < A[i]) {", "if (B[j] <= A[i]) {", 2),
     ("f32_drops_B_tail", "    while (j < n) C[k++] = B[j++];\n", "\n", 2),
+    ("keys_i64_unsigned_compare", "        int64_t x = ((const int64_t *)A)[i], y = ((const int64_t *)B)[j];",
+     "        uint64_t x = ((const int64_t *)A)[i], y = ((const int64_t *)B)[j];", 0),
+    ("keys_u64_signed_compare", "        uint64_t x = ((const uint64_t *)A)[i], y = ((const uint64_t *)B)[j];",
+     "        int64_t x = ((const uint64_t *)A)[i], y = ((const uint64_t *)B)[j];", 0),
+    ("keys_f64_compared_as_bits", "        double x = ((const double *)A)[i], y = ((const double *)B)[j];",
+     "        int64_t x = ((const int64_t *)A)[i], y = ((const int64_t *)B)[j];", 0),
+    ("keys_f32_desc_B_first_on_tie", "return desc ? (y > x) : (y < x);", "return desc ? (y >= x) : (y < x);", 2),
+    ("keys_f64_desc_B_first_on_tie", "return desc ? (y > x) : (y < x);", "return desc ? (y >= x) : (y < x);", 5),
+    ("keys_i32_desc_reversed", "return desc ? (y > x) : (y < x);", "return desc ? (y < x) : (y < x);", 0),
+    ("keys_drops_B_tail", "    for (; j < n; ++j, ++k) memcpy(c + (size_t)k * e, b + (size_t)j * e, e);\n", "\n", 0),
     ("sort_stops_one_pass_early", "for (int64_t width = 1; width < n; width *= 2) {", "for (int64_t width = 2; width < n; width *= 2) {", 0),
 ]
 
@@ -77,6 +87,8 @@ for check in ALL_CHECKS:
             check(lib, max_len=4)
         elif check.__name__ == "check_typed_keys":
             check(lib, max_len=3)
+        elif check.__name__ == "check_merge_keys":
+            check(lib, max_len=3, limit=25)
         else:
             check(lib)
     except Exception:

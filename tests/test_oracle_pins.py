@@ -269,6 +269,91 @@ def check_typed_keys(lib, max_len=4):
         assert np.array_equal(got.view(np.uint32), fcat[np.argsort(fcat, kind="stable")].view(np.uint32))
 
 
+_KEY_ALPHABETS = {
+    np.int32: [np.iinfo(np.int32).min, -1, 0, 1, np.iinfo(np.int32).max],
+    np.uint32: [0, 1, 0x7FFFFFFF, 0x80000000, 0xFFFFFFFF],
+    np.float32: [-np.inf, -1.5, -0.0, 0.0, 1e-45, np.inf],
+    np.int64: [np.iinfo(np.int64).min, -(1 << 32), -1, 0, 1 << 32, np.iinfo(np.int64).max],
+    np.uint64: [0, 1, (1 << 63) - 1, 1 << 63, (1 << 64) - 1],
+    np.float64: [-np.inf, -2.5e300, -0.0, 0.0, 5e-324, np.inf],
+}
+
+
+def _sorted_inputs(values, dtype, max_len, descending, rng, limit):
+    """Sorted sequences (in the merge order) over `values`, as bit patterns:
+    every arrangement the order allows, including -0.0 / +0.0 in either
+    order, sampled down to `limit`."""
+    arr = np.array(values, dtype=dtype)
+    ubits = {4: np.uint32, 8: np.uint64}[arr.itemsize]
+    pats = [int(b) for b in arr.view(ubits)]
+    num = {p: arr[t].item() for t, p in enumerate(pats)}
+    seqs = []
+    for L in range(max_len + 1):
+        for combo in itertools.product(pats, repeat=L):
+            vals = [num[p] for p in combo]
+            ok = all((vals[t] >= vals[t + 1]) if descending else (vals[t] <= vals[t + 1]) for t in range(L - 1))
+            if ok:
+                seqs.append(list(combo))
+    if len(seqs) > limit:
+        keep = rng.choice(len(seqs), size=limit, replace=False)
+        seqs = [seqs[int(t)] for t in keep] + [[]]
+    return seqs, num, ubits
+
+
+def _stable_desc_order(x):
+    """Indices of a stable descending sort, from numpy's stable ascending
+    argsort: sort the reversed array, reverse the result, map back."""
+    r = np.argsort(x[::-1], kind="stable")[::-1]
+    return x.size - 1 - r
+
+
+def check_merge_keys(lib, max_len=3, limit=60):
+    """O1 for all six key types, ascending and descending.
+
+    Brute force: every pair of sorted inputs (sampled) over an alphabet of
+    the type's extremes (sign bits, -0.0 and +0.0, subnormals, infinities)
+    equals Python's stable sort of the concatenation by numeric value, bit
+    for bit; sorted(..., reverse=True) is documented stable, so descending
+    ties keep A first.  A wrong compare type (signed for unsigned, bits for
+    floats), a flipped tie rule or a reversed order each fails here.  Random
+    inputs: equal to numpy's stable argsort of the concatenation (for
+    descending, through the reversal construction above)."""
+    rng = np.random.default_rng(23)
+    for dtype, alpha in _KEY_ALPHABETS.items():
+        for desc in (False, True):
+            seqs, num, ubits = _sorted_inputs(alpha, dtype, max_len, desc, rng, limit)
+            for A in seqs:
+                for B in seqs:
+                    tagged = sorted([(num[p], p) for p in A] + [(num[p], p) for p in B],
+                                    key=lambda t: t[0], reverse=desc)
+                    want = [p for _, p in tagged]
+                    a = np.array(A, dtype=ubits).view(dtype)
+                    b = np.array(B, dtype=ubits).view(dtype)
+                    got = oracle.merge_keys(a, b, descending=desc, lib=lib)
+                    assert [int(x) for x in got.view(ubits)] == want, (dtype, desc, A, B)
+            for m, n in [(0, 9), (9, 0), (500, 700), (2049, 31)]:
+                src = np.array(alpha, dtype=dtype)
+                a = src[rng.integers(0, src.size, m)]
+                b = src[rng.integers(0, src.size, n)]
+                if np.issubdtype(dtype, np.integer):
+                    info = np.iinfo(dtype)
+                    a = np.concatenate([a[: m // 2], rng.integers(info.min, info.max, m - m // 2, dtype=dtype,
+                                                                  endpoint=True)]) if m else a
+                    b = np.concatenate([b[: n // 2], rng.integers(info.min, info.max, n - n // 2, dtype=dtype,
+                                                                  endpoint=True)]) if n else b
+                else:
+                    a = (a * rng.integers(1, 5, m)).astype(dtype)
+                    b = (b * rng.integers(1, 5, n)).astype(dtype)
+                a = np.sort(a, kind="stable")
+                b = np.sort(b, kind="stable")
+                if desc:
+                    a, b = a[::-1].copy(), b[::-1].copy()
+                cat = np.concatenate([a, b])
+                order = _stable_desc_order(cat) if desc else np.argsort(cat, kind="stable")
+                got = oracle.merge_keys(a, b, descending=desc, lib=lib)
+                assert np.array_equal(got.view(ubits), cat[order].view(ubits)), (dtype, desc, m, n)
+
+
 ALL_CHECKS = [
     check_worked_example,
     check_tie_case,
@@ -278,6 +363,7 @@ ALL_CHECKS = [
     check_invariants_random,
     check_merge_sort,
     check_typed_keys,
+    check_merge_keys,
 ]
 
 
