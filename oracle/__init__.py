@@ -12,7 +12,8 @@ Functions (see ``merge_oracle.c`` for the definition each one restates):
   :func:`merge_pairs_u32` -- two-pointer stable merge (O1)
 * :func:`corank_pages` -- the pages' co-rank bisection, with trace (O2)
 * :func:`corank_count` -- co-rank by counting merge steps (O3)
-* :func:`merge_sort_pairs_u32` -- bottom-up stable merge sort from O1 (O4)
+* :func:`merge_sort_pairs_u32`, :func:`merge_sort_keys` -- bottom-up stable
+  merge sort from O1 (O4)
 * :func:`merge_at_i32` -- one output element C[k] via O2 (O5)
 """
 from __future__ import annotations
@@ -77,6 +78,8 @@ def _declare(lib):
     lib.oracle_merge_f32.restype = None
     lib.oracle_merge_keys.argtypes = [ctypes.c_int, ctypes.c_int, _P, _I64, _P, _I64, _P]
     lib.oracle_merge_keys.restype = ctypes.c_int
+    lib.oracle_merge_sort_keys.argtypes = [ctypes.c_int, ctypes.c_int, _P, _P, _I64]
+    lib.oracle_merge_sort_keys.restype = ctypes.c_int
     lib.oracle_merge_pairs_u32.argtypes = [_P, _P, _I64, _P, _P, _I64, _P, _P]
     lib.oracle_merge_pairs_u32.restype = None
     lib.oracle_corank_pages_i32.argtypes = [_I64, _P, _I64, _P, _I64, _P, _I64, _P]
@@ -222,4 +225,22 @@ def merge_sort_pairs_u32(keys, vals, lib=None):
     rc = lib.oracle_merge_sort_pairs_u32(_ptr(k), _ptr(v), k.size)
     if rc != 0:
         raise MemoryError("oracle merge sort could not allocate its scratch")
+    return k, v
+
+
+def merge_sort_keys(keys, vals=None, descending=False, lib=None):
+    """O4 for any of the six key types (from keys' dtype), either order;
+    optional uint32 values.  Returns sorted copies (keys, vals or None)."""
+    lib = lib or load()
+    k = np.array(keys, copy=True)
+    if k.dtype not in KEY_CODES:
+        raise ValueError(f"no oracle key type for {k.dtype}")
+    v = None if vals is None else np.array(vals, dtype=np.uint32, copy=True)
+    assert v is None or v.size == k.size
+    rc = lib.oracle_merge_sort_keys(KEY_CODES[k.dtype], 1 if descending else 0, _ptr(k),
+                                    None if v is None else _ptr(v), k.size)
+    if rc == -2:
+        raise MemoryError("oracle merge sort could not allocate its scratch")
+    if rc != 0:
+        raise ValueError("oracle_merge_sort_keys rejected the key type")
     return k, v

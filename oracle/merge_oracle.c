@@ -27,8 +27,9 @@
  *       stable merge for k outputs and count how many came from A
  *       ([P1] §Co-rank Function 定義與不變式; [P4] coRank comment:
  *       "a[0..i) and b[0..j) are exactly the k smallest elements").
- *   O4  oracle_merge_sort_pairs_u32: bottom-up stable merge sort built only
- *       from O1 (runs of one, doubling), as in [P3] (merge-sort stages).
+ *   O4  oracle_merge_sort_pairs_u32 / oracle_merge_sort_keys: bottom-up
+ *       stable merge sort built only from O1 (runs of one, doubling), as in
+ *       [P3] (merge-sort stages).
  *   O5  oracle_merge_at_i32: one output element C[k] from O2's split and one
  *       two-pointer step; used for sampled checks at sizes where a full merge
  *       is not wanted.
@@ -158,8 +159,12 @@ static int oracle_b_before_a(int type, int desc, const void *A, int64_t i,
     }
 }
 
-int oracle_merge_keys(int type, int desc, const void *A, int64_t m,
-                      const void *B, int64_t n, void *C)
+/* The merge above with optional uint32 values that travel with their keys
+ * (va, vb, vc all NULL for keys only). */
+static int oracle_merge_keys_vals(int type, int desc, const void *A,
+                                  const uint32_t *va, int64_t m, const void *B,
+                                  const uint32_t *vb, int64_t n, void *C,
+                                  uint32_t *vc)
 {
     const size_t e = oracle_key_size(type);
     const unsigned char *a = (const unsigned char *)A;
@@ -170,16 +175,30 @@ int oracle_merge_keys(int type, int desc, const void *A, int64_t m,
     while (i < m && j < n) {
         if (oracle_b_before_a(type, desc, A, i, B, j)) {
             memcpy(c + (size_t)k * e, b + (size_t)j * e, e);
+            if (vc != NULL) vc[k] = vb[j];
             ++j;
         } else {
             memcpy(c + (size_t)k * e, a + (size_t)i * e, e);
+            if (vc != NULL) vc[k] = va[i];
             ++i;
         }
         ++k;
     }
-    for (; i < m; ++i, ++k) memcpy(c + (size_t)k * e, a + (size_t)i * e, e);
-    for (; j < n; ++j, ++k) memcpy(c + (size_t)k * e, b + (size_t)j * e, e);
+    for (; i < m; ++i, ++k) {
+        memcpy(c + (size_t)k * e, a + (size_t)i * e, e);
+        if (vc != NULL) vc[k] = va[i];
+    }
+    for (; j < n; ++j, ++k) {
+        memcpy(c + (size_t)k * e, b + (size_t)j * e, e);
+        if (vc != NULL) vc[k] = vb[j];
+    }
     return 0;
+}
+
+int oracle_merge_keys(int type, int desc, const void *A, int64_t m,
+                      const void *B, int64_t n, void *C)
+{
+    return oracle_merge_keys_vals(type, desc, A, NULL, m, B, NULL, n, C, NULL);
 }
 
 /* Same rule on unsigned keys; each value travels with its key. */
@@ -377,6 +396,49 @@ int oracle_merge_sort_pairs_u32(uint32_t *keys, uint32_t *vals, int64_t n)
     if (src_k != keys) {
         memcpy(keys, src_k, (size_t)n * sizeof(uint32_t));
         memcpy(vals, src_v, (size_t)n * sizeof(uint32_t));
+    }
+    free(tk);
+    free(tv);
+    return 0;
+}
+
+/*
+ * O4 for the key types of oracle_merge_keys, either order: the same
+ * bottom-up stable merge sort (runs of one, doubling; the earlier run is A),
+ * each merge being O1 on typed keys.  vals (uint32, may be NULL) travel with
+ * their keys.  Returns 0, -1 for an unknown type, -2 if scratch cannot be
+ * allocated.
+ */
+int oracle_merge_sort_keys(int type, int desc, void *keys, uint32_t *vals,
+                           int64_t n)
+{
+    const size_t e = oracle_key_size(type);
+    if (e == 0) return -1;
+    if (n <= 1) return 0;
+    unsigned char *tk = (unsigned char *)malloc((size_t)n * e);
+    uint32_t *tv = vals != NULL ? (uint32_t *)malloc((size_t)n * sizeof(uint32_t)) : NULL;
+    if (tk == NULL || (vals != NULL && tv == NULL)) {
+        free(tk);
+        free(tv);
+        return -2;
+    }
+    unsigned char *src_k = (unsigned char *)keys, *dst_k = tk;
+    uint32_t *src_v = vals, *dst_v = tv;
+    for (int64_t width = 1; width < n; width *= 2) {
+        for (int64_t lo = 0; lo < n; lo += 2 * width) {
+            int64_t mid = (lo + width < n) ? lo + width : n;
+            int64_t hi = (lo + 2 * width < n) ? lo + 2 * width : n;
+            oracle_merge_keys_vals(type, desc,
+                                   src_k + (size_t)lo * e, src_v ? src_v + lo : NULL, mid - lo,
+                                   src_k + (size_t)mid * e, src_v ? src_v + mid : NULL, hi - mid,
+                                   dst_k + (size_t)lo * e, dst_v ? dst_v + lo : NULL);
+        }
+        unsigned char *t = src_k; src_k = dst_k; dst_k = t;
+        uint32_t *tq = src_v; src_v = dst_v; dst_v = tq;
+    }
+    if (src_k != (unsigned char *)keys) {
+        memcpy(keys, src_k, (size_t)n * e);
+        if (vals != NULL) memcpy(vals, src_v, (size_t)n * sizeof(uint32_t));
     }
     free(tk);
     free(tv);

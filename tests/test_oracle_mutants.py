@@ -55,7 +55,12 @@ MUTANTS = [
     ("keys_f32_desc_B_first_on_tie", "return desc ? (y > x) : (y < x);", "return desc ? (y >= x) : (y < x);", 2),
     ("keys_f64_desc_B_first_on_tie", "return desc ? (y > x) : (y < x);", "return desc ? (y >= x) : (y < x);", 5),
     ("keys_i32_desc_reversed", "return desc ? (y > x) : (y < x);", "return desc ? (y < x) : (y < x);", 0),
-    ("keys_drops_B_tail", "    for (; j < n; ++j, ++k) memcpy(c + (size_t)k * e, b + (size_t)j * e, e);\n", "\n", 0),
+    ("keys_drops_B_tail", "    for (; j < n; ++j, ++k) {\n        memcpy(c + (size_t)k * e, b + (size_t)j * e, e);\n        if (vc != NULL) vc[k] = vb[j];\n    }\n", "\n", 0),
+    ("sort_keys_later_run_first",
+     "src_k + (size_t)lo * e, src_v ? src_v + lo : NULL, mid - lo,\n                                   src_k + (size_t)mid * e, src_v ? src_v + mid : NULL, hi - mid,",
+     "src_k + (size_t)mid * e, src_v ? src_v + mid : NULL, hi - mid,\n                                   src_k + (size_t)lo * e, src_v ? src_v + lo : NULL, mid - lo,", 0),
+    ("sort_keys_drops_B_values", "        if (vc != NULL) vc[k] = vb[j];\n    }", "    }", 0),
+    ("sort_keys_stops_one_pass_early", "for (int64_t width = 1; width < n; width *= 2) {", "for (int64_t width = 2; width < n; width *= 2) {", 1),
     ("sort_stops_one_pass_early", "for (int64_t width = 1; width < n; width *= 2) {", "for (int64_t width = 2; width < n; width *= 2) {", 0),
 ]
 
@@ -89,6 +94,8 @@ for check in ALL_CHECKS:
             check(lib, max_len=3)
         elif check.__name__ == "check_merge_keys":
             check(lib, max_len=3, limit=25)
+        elif check.__name__ == "check_merge_sort_keys":
+            check(lib, max_len=4)
         else:
             check(lib)
     except Exception:

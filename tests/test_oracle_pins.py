@@ -354,6 +354,45 @@ def check_merge_keys(lib, max_len=3, limit=60):
                 assert np.array_equal(got.view(ubits), cat[order].view(ubits)), (dtype, desc, m, n)
 
 
+def check_merge_sort_keys(lib, max_len=5):
+    """O4 on all six key types, both orders, with and without values.
+
+    Brute force: every sequence up to max_len over three keys of the type
+    (for floats -0.0, +0.0 and 1.0, so equal keys with different bits show
+    whether input order is kept) sorts as Python's stable sorted() by value
+    (reverse=True is documented stable).  Random inputs with heavy ties and
+    the type's extremes: keys (bit for bit) and values equal the
+    permutation of numpy's stable argsort (descending through the reversal
+    construction)."""
+    rng = np.random.default_rng(29)
+    for dtype, alpha in _KEY_ALPHABETS.items():
+        arr = np.array(alpha, dtype=dtype)
+        ubits = {4: np.uint32, 8: np.uint64}[arr.itemsize]
+        small = np.array([-0.0, 0.0, 1.0] if arr.dtype.kind == "f" else [alpha[0], alpha[2], alpha[-1]], dtype=dtype)
+        for desc in (False, True):
+            for L in range(max_len + 1):
+                for combo in itertools.product(range(3), repeat=L):
+                    keys = small[list(combo)]
+                    tags = np.arange(L, dtype=np.uint32)
+                    want = sorted(zip(keys.tolist(), keys.view(ubits).tolist(), tags.tolist()),
+                                  key=lambda t: t[0], reverse=desc)
+                    gk, gv = oracle.merge_sort_keys(keys, tags, descending=desc, lib=lib)
+                    assert gk.view(ubits).tolist() == [w[1] for w in want], (dtype, desc, combo)
+                    assert gv.tolist() == [w[2] for w in want], (dtype, desc, combo)
+            for n in [0, 1, 2, 7, 100, 1000, 4099]:
+                keys = arr[rng.integers(0, arr.size, n)]
+                if arr.dtype.kind in "iu" and n > 4:
+                    info = np.iinfo(dtype)
+                    keys[: n // 2] = rng.integers(info.min, info.max, n // 2, dtype=dtype, endpoint=True)
+                vals = np.arange(n, dtype=np.uint32)
+                order = _stable_desc_order(keys) if desc else np.argsort(keys, kind="stable")
+                gk, gv = oracle.merge_sort_keys(keys, vals, descending=desc, lib=lib)
+                assert np.array_equal(gk.view(ubits), keys[order].view(ubits)), (dtype, desc, n)
+                assert np.array_equal(gv, vals[order]), (dtype, desc, n)
+                gk2, none = oracle.merge_sort_keys(keys, None, descending=desc, lib=lib)
+                assert none is None and np.array_equal(gk2.view(ubits), gk.view(ubits))
+
+
 ALL_CHECKS = [
     check_worked_example,
     check_tie_case,
@@ -364,6 +403,7 @@ ALL_CHECKS = [
     check_merge_sort,
     check_typed_keys,
     check_merge_keys,
+    check_merge_sort_keys,
 ]
 
 
