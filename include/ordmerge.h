@@ -165,6 +165,42 @@ uint64_t om_launch_count(void);
 om_status om_merge_i32_noalloc(const int32_t *A, int64_t m, const int32_t *B,
                                int64_t n, int32_t *C, void *stream);
 
+/* ---- other key types and descending order ------------------------------ */
+
+/* Key types of om_merge_keys (element size 4 or 8 bytes). */
+typedef enum {
+    OM_KEY_I32 = 0, /* int32, signed order */
+    OM_KEY_U32 = 1, /* uint32, unsigned order */
+    OM_KEY_F32 = 2, /* IEEE binary32, numeric order */
+    OM_KEY_I64 = 3, /* int64, signed order */
+    OM_KEY_U64 = 4, /* uint64, unsigned order */
+    OM_KEY_F64 = 5  /* IEEE binary64, numeric order */
+} om_key_type;
+
+typedef enum {
+    OM_ASCENDING = 0,  /* inputs and output nondecreasing */
+    OM_DESCENDING = 1  /* inputs and output nonincreasing */
+} om_order;
+
+/*
+ * C[0 .. m+n) = stable merge of the keys A[0..m) and B[0..n) of type
+ * `key_type`, both sorted in `order`; ties take A first in either order.
+ * The same partition and tile-merge kernels as om_merge_i32, for another
+ * element size and comparison.  ("merge_path.cu" runs the method on float
+ * keys; the co-rank test of "Co-rank Function 實作與 Basic Parallel Merge
+ * Kernel", §Important, with <= and < read in the merge order.)
+ *  - Floating-point keys compare by value: -0.0 and +0.0 are equal (so the
+ *    A one comes first) and keep their bits.  NaN has no place in a sorted
+ *    array; input holding NaN counts as unsorted (output unspecified, every
+ *    kernel still terminates).
+ *  - A, B and C must be aligned to the key size (4 or 8 bytes) and C must
+ *    not overlap A or B.
+ *  - An unknown key_type or order is OM_EINVAL.  Other rules and errors are
+ *    those of om_merge_i32.
+ */
+om_status om_merge_keys(int key_type, int order, const void *A, int64_t m,
+                        const void *B, int64_t n, void *C, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

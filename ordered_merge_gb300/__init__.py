@@ -23,6 +23,10 @@ OM_OK, OM_EINVAL, OM_ERANGE, OM_ENOMEM, OM_ECUDA, OM_EDEVICE = range(6)
 
 KIND_PARTITION, KIND_TILE_MERGE, KIND_BLOCK_SORT, KIND_CORANK = range(4)
 
+# om_key_type codes and their element sizes
+KEY_TYPES = {"i32": (0, 4), "u32": (1, 4), "f32": (2, 4), "i64": (3, 8), "u64": (4, 8), "f64": (5, 8)}
+OM_ASCENDING, OM_DESCENDING = 0, 1
+
 
 class OrdMergeError(RuntimeError):
     def __init__(self, status: int, what: str):
@@ -58,6 +62,8 @@ def _load():
     lib.om_trace_reset.restype = I32
     lib.om_trace_read.argtypes = [I32, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)]
     lib.om_trace_read.restype = I32
+    lib.om_merge_keys.argtypes = [I32, I32, P, I64, P, I64, P, P]
+    lib.om_merge_keys.restype = I32
     lib.om_launch_count.argtypes = []
     lib.om_launch_count.restype = ctypes.c_uint64
     return lib
@@ -141,6 +147,55 @@ def om_merge_i32(A, B, C=None, stream=None):
     return C
 
 
+def _key_type_of(dtype) -> str:
+    import torch
+
+    names = {torch.int32: "i32", torch.float32: "f32", torch.int64: "i64", torch.float64: "f64"}
+    for extra, name in (("uint32", "u32"), ("uint64", "u64")):
+        if hasattr(torch, extra):
+            names[getattr(torch, extra)] = name
+    if dtype not in names:
+        raise ValueError(f"no key type for {dtype}; pass key_type")
+    return names[dtype]
+
+
+def _ptr_sized(t, name: str, size: int):
+    """Device pointer of a contiguous CUDA tensor of `size`-byte elements."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.element_size() != size:
+        raise ValueError(f"{name} must have {size}-byte elements (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr() if t.numel() else None
+
+
+def om_merge_keys(A, B, C=None, key_type=None, descending=False, stream=None):
+    """C = stable merge of sorted device tensors A and B (ties: A first).
+
+    key_type: "i32", "u32", "f32", "i64", "u64" or "f64" (default: from
+    A's dtype); the tensors' bits are read as that type, so an int32 tensor
+    can carry uint32 keys.  descending: inputs and output nonincreasing.
+    """
+    import torch
+
+    name = key_type or _key_type_of(A.dtype)
+    if name not in KEY_TYPES:
+        raise ValueError(f"unknown key type {name!r}")
+    code, size = KEY_TYPES[name]
+    if C is None:
+        C = torch.empty(A.numel() + B.numel(), dtype=A.dtype, device=A.device)
+    if C.numel() != A.numel() + B.numel():
+        raise ValueError("C must hold len(A) + len(B) elements")
+    _check(
+        _lib.om_merge_keys(code, OM_DESCENDING if descending else OM_ASCENDING, _ptr_sized(A, "A", size),
+                           A.numel(), _ptr_sized(B, "B", size), B.numel(), _ptr_sized(C, "C", size),
+                           _stream(stream)),
+        "om_merge_keys",
+    )
+    return C
+
+
 def om_merge_pairs_u32(keysA, valsA, keysB, valsB, keysC=None, valsC=None, stream=None):
     """Stable merge of (uint32 key, uint32 value) pairs; keys compared unsigned.
 
@@ -212,5 +267,6 @@ corank_i32 = om_corank_i32
 corank_i32_batch = om_corank_i32_batch
 merge_i32 = om_merge_i32
 merge_pairs_u32 = om_merge_pairs_u32
+merge_keys = om_merge_keys
 merge_sort_u32 = om_merge_sort_u32
 device_error = om_device_error

@@ -9,33 +9,11 @@
 
 #include <cuda_runtime.h>
 
-#include "merge_kernels.cuh"
-#include "ordmerge.h"
+#include "api_internal.cuh"
 #include "sort_kernels.cuh"
 
 namespace om {
 
-// Kernel configurations (consumer threads, outputs per thread, log2 ring,
-// log2 chunk; every CTA has two more warps for the producers).
-//  merge: 128 consumers x 23 outputs = 2944 outputs per sub-tile; 4096-element
-//         rings per side refilled in 1024-element (4 KB) chunks; 45 KB of
-//         shared memory, 5 CTAs per SM.  (Measured on GB300 against 1920- and
-//         2432-output sub-tiles, 512/2048-element chunks, 8192-element rings
-//         and 64- to 256-thread CTAs: per-sub-tile and per-chunk work
-//         dominates, so the largest sub-tile and chunk that fit a 4096 ring win.)
-using MergeCfg = TileCfg<128, 23, 12, 10>;
-//  key+value merge: four rings (keys and values of A and B), so smaller rings
-//  keep 5 CTAs per SM: 128 x 11 = 1408 outputs per sub-tile, 2048-element
-//  rings, 512-element chunks (best of the shapes measured on GB300).
-using PairsCfg = TileCfg<128, 11, 11, 9>;
-template <bool V>
-struct CfgFor {
-    using type = MergeCfg;
-};
-template <>
-struct CfgFor<true> {
-    using type = PairsCfg;
-};
 //  sort: one block pass sorts 256 x 16 = 4096-element tiles in shared memory
 //        (runs of 16 in registers, then merges of whole pairs of runs per
 //        CTA through 1024 to 4096); later passes use
@@ -43,21 +21,10 @@ struct CfgFor<true> {
 using SmallMergeCfg = BlockSortCfg<256, 16>;
 constexpr int kEarlyTo = SmallMergeCfg::TILE;  // runs after the block pass: 4096
 
-enum KernelKind { kKindPartition = 0, kKindTileMerge = 1, kKindBlockSort = 2, kKindCorank = 3, kNumKinds = 4 };
-
 // ------------------------------------------------------------ device state --
 
 static __device__ uint32_t g_error_word;
 static __device__ int64_t g_corank_slot;
-
-struct DeviceState {
-    bool ready = false;
-    int sm_count = 0;
-    int resident_merge = 0;  // tile-merge CTAs resident per SM (keys only / with values)
-    int resident_merge_v = 0;
-    uint32_t* err = nullptr;
-    int64_t* corank_slot = nullptr;
-};
 
 static std::mutex g_mu;
 static DeviceState g_devices[128];
@@ -69,9 +36,7 @@ static cudaError_t set_smem(F* kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-// Per-device set-up, once: SM count, addresses of the library's device
-// words, shared-memory limits of the kernels.
-static om_status device_state(DeviceState** out) {
+om_status device_state(DeviceState** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return OM_ECUDA;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -83,18 +48,18 @@ static om_status device_state(DeviceState** out) {
         if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.corank_slot), g_corank_slot) != cudaSuccess)
             return OM_ECUDA;
         cudaError_t e = cudaSuccess;
-        e = e ? e : set_smem(tile_merge_kernel<MergeCfg, int32_t, false>, TileSmem<MergeCfg, false>::total);
-        e = e ? e : set_smem(tile_merge_kernel<MergeCfg, uint32_t, false>, TileSmem<MergeCfg, false>::total);
-        e = e ? e : set_smem(tile_merge_kernel<PairsCfg, uint32_t, true>, TileSmem<PairsCfg, true>::total);
+        e = e ? e : set_smem(tile_merge_kernel<MergeCfg, int32_t, false>, SmemFor<int32_t, false>::total);
+        e = e ? e : set_smem(tile_merge_kernel<MergeCfg, uint32_t, false>, SmemFor<uint32_t, false>::total);
+        e = e ? e : set_smem(tile_merge_kernel<PairsCfg, uint32_t, true>, SmemFor<uint32_t, true>::total);
         e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, true>, block_sort_smem_bytes<SmallMergeCfg, true>());
         e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, false>, block_sort_smem_bytes<SmallMergeCfg, false>());
         if (e != cudaSuccess) return OM_ECUDA;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge,
                                                           tile_merge_kernel<MergeCfg, int32_t, false>,
-                                                          MergeCfg::THREADS, TileSmem<MergeCfg, false>::total);
+                                                          MergeCfg::THREADS, SmemFor<int32_t, false>::total);
         e = e ? e : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge_v,
                                                                    tile_merge_kernel<PairsCfg, uint32_t, true>,
-                                                                   PairsCfg::THREADS, TileSmem<PairsCfg, true>::total);
+                                                                   PairsCfg::THREADS, SmemFor<uint32_t, true>::total);
         if (e != cudaSuccess) return OM_ECUDA;
         if (d.resident_merge < 1) d.resident_merge = 1;
         if (d.resident_merge_v < 1) d.resident_merge_v = 1;
@@ -105,11 +70,6 @@ static om_status device_state(DeviceState** out) {
 }
 
 // ----------------------------------------------------------------- tracing --
-
-struct TraceRec {
-    int kind;
-    cudaEvent_t e0, e1;
-};
 
 static std::mutex g_trace_mu;
 static bool g_trace_on = false;
@@ -129,22 +89,22 @@ static cudaEvent_t pool_event() {
     return e;
 }
 
-// Launches through `launch` (a callable issuing exactly one kernel), counting
-// it and, with tracing on, bracketing it with events on `stream`.
-template <typename F>
-static cudaError_t traced(int kind, cudaStream_t stream, F&& launch) {
-    TraceRec rec{kind, nullptr, nullptr};
+bool trace_begin(int kind, cudaStream_t stream, TraceRec* rec) {
+    rec->kind = kind;
     bool on;
     {
         std::lock_guard<std::mutex> lk(g_trace_mu);
         on = g_trace_on;
         if (on) {
-            rec.e0 = pool_event();
-            rec.e1 = pool_event();
+            rec->e0 = pool_event();
+            rec->e1 = pool_event();
         }
     }
-    if (on) cudaEventRecord(rec.e0, stream);
-    launch();
+    if (on) cudaEventRecord(rec->e0, stream);
+    return on;
+}
+
+cudaError_t trace_end(const TraceRec& rec, bool on, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (on) {
@@ -170,15 +130,6 @@ static void trace_collect_locked() {
 
 // ------------------------------------------------------------------ helpers --
 
-static bool misaligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) != 0; }
-
-static bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
-    if (na <= 0 || nb <= 0) return false;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), a1 = a0 + (uintptr_t)na * 4;
-    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + (uintptr_t)nb * 4;
-    return a0 < b1 && b0 < a1;
-}
-
 static int64_t env_int(const char* name, int64_t fallback) {
     const char* s = std::getenv(name);
     if (s == nullptr || *s == 0) return fallback;
@@ -192,61 +143,12 @@ static int64_t env_int(const char* name, int64_t fallback) {
 // number of waves of resident CTAs (OM_WAVES, default 1) so that no SM idles
 // through a partial last wave.  Long ranges also amortise each CTA's start-up
 // (the latency of its first chunks).  OM_SUBTILES_PER_RANGE overrides.
-static int64_t subtiles_per_range(int64_t subtiles, int64_t resident_ctas) {
+int64_t subtiles_per_range(int64_t subtiles, int64_t resident_ctas) {
     const int64_t waves = env_int("OM_WAVES", 1);
     const int64_t slots = resident_ctas * waves;
     int64_t s = (subtiles + slots - 1) / slots;
     if (s < 1) s = 1;
     return env_int("OM_SUBTILES_PER_RANGE", s);
-}
-
-static om_status cuda_fail(cudaError_t e) {
-    return e == cudaErrorMemoryAllocation ? OM_ENOMEM : OM_ECUDA;
-}
-
-// Partition + tile-merge launches for one geometry (split has nranges + 1
-// slots of scratch).
-template <typename K, bool V>
-static cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const DeviceState* d, cudaStream_t st) {
-    using Cfg = typename CfgFor<V>::type;
-    using Smem = TileSmem<Cfg, V>;
-    const unsigned pgrid = (unsigned)((g.nranges + 3) / 4);  // one warp per range
-    cudaError_t e = traced(kKindPartition, st, [&] { partition_kernel<K, V><<<pgrid, 128, 0, st>>>(g, split); });
-    if (e != cudaSuccess) return e;
-    return traced(kKindTileMerge, st, [&] {
-        tile_merge_kernel<Cfg, K, V><<<(unsigned)g.nranges, Cfg::THREADS, Smem::total, st>>>(g, split, d->err);
-    });
-}
-
-
-
-
-
-
-template <typename K, bool V>
-static om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, const uint32_t* bv,
-                            int64_t n, K* ck, uint32_t* cv, cudaStream_t st) {
-    DeviceState* d = nullptr;
-    om_status s = device_state(&d);
-    if (s != OM_OK) return s;
-    using Cfg = typename CfgFor<V>::type;
-    const int64_t total = m + n;
-    const int64_t subtiles = (total + Cfg::T - 1) / Cfg::T;
-    const int64_t resident = (int64_t)d->sm_count * (V ? d->resident_merge_v : d->resident_merge);
-    const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
-    const int64_t nranges = (total + range_len - 1) / range_len;
-    if (nranges > 0x7fffffff) return OM_ERANGE;
-    MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
-    int64_t* split = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&split), (size_t)(nranges + 1) * 8, st);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return OM_ENOMEM;
-    }
-    e = launch_merge<K, V>(g, split, d, st);
-    cudaError_t ef = cudaFreeAsync(split, st);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return ef == cudaSuccess ? OM_OK : OM_ECUDA;
 }
 
 template <bool V>
@@ -261,7 +163,7 @@ static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream
     // passes after the block pass.
     int passes = 0;
     for (int64_t r = kEarlyTo; r < n; r *= 2) ++passes;
-    using Cfg = typename CfgFor<V>::type;
+    using Cfg = typename CfgFor<uint32_t, V>::type;
     const int64_t subtiles = (n + Cfg::T - 1) / Cfg::T;
     const int64_t resident = (int64_t)d->sm_count * (V ? d->resident_merge_v : d->resident_merge);
     const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
@@ -378,7 +280,11 @@ om_status om_merge_i32(const int32_t* A, int64_t m, const int32_t* B, int64_t n,
     if ((m > 0 && A == nullptr) || (n > 0 && B == nullptr) || C == nullptr) return OM_EINVAL;
     if (misaligned4(A) || misaligned4(B) || misaligned4(C)) return OM_EINVAL;
     if (overlaps(C, total, A, m) || overlaps(C, total, B, n)) return OM_EINVAL;
-    return merge_impl<int32_t, false>(A, nullptr, m, B, nullptr, n, C, nullptr, (cudaStream_t)stream);
+    DeviceState* d = nullptr;
+    const om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    return merge_impl<int32_t, false>(A, nullptr, m, B, nullptr, n, C, nullptr, d->resident_merge,
+                                      (cudaStream_t)stream);
 }
 
 om_status om_merge_pairs_u32(const uint32_t* keysA, const uint32_t* valsA, int64_t m, const uint32_t* keysB,
@@ -402,7 +308,11 @@ om_status om_merge_pairs_u32(const uint32_t* keysA, const uint32_t* valsA, int64
         if (overlaps(out, total, keysA, m) || overlaps(out, total, valsA, m) || overlaps(out, total, keysB, n) ||
             overlaps(out, total, valsB, n))
             return OM_EINVAL;
-    return merge_impl<uint32_t, true>(keysA, valsA, m, keysB, valsB, n, keysC, valsC, (cudaStream_t)stream);
+    DeviceState* d = nullptr;
+    const om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    return merge_impl<uint32_t, true>(keysA, valsA, m, keysB, valsB, n, keysC, valsC, d->resident_merge_v,
+                                      (cudaStream_t)stream);
 }
 
 om_status om_merge_sort_u32(uint32_t* keys, uint32_t* vals, int64_t n, void* stream) {

@@ -1,0 +1,162 @@
+// Internal interface shared by the library's translation units (not part of
+// the C ABI): kernel configurations, per-device state, launch counting and
+// tracing, argument helpers and the partition + tile-merge launch.
+#pragma once
+
+#include <cstdint>
+#include <cstdlib>
+
+#include <cuda_runtime.h>
+
+#include "merge_kernels.cuh"
+#include "ordmerge.h"
+
+namespace om {
+
+// Kernel configurations (consumer threads, outputs per thread, log2 ring,
+// log2 chunk; every CTA has two more warps for the producers).
+//  merge: 128 consumers x 23 outputs = 2944 outputs per sub-tile; 4096-element
+//         rings per side refilled in 1024-element (4 KB) chunks; 45 KB of
+//         shared memory, 5 CTAs per SM.  (Measured on GB300 against 1920- and
+//         2432-output sub-tiles, 512/2048-element chunks, 8192-element rings
+//         and 64- to 256-thread CTAs: per-sub-tile and per-chunk work
+//         dominates, so the largest sub-tile and chunk that fit a 4096 ring win.)
+using MergeCfg = TileCfg<128, 23, 12, 10>;
+//  key+value merge: four rings (keys and values of A and B), so smaller rings
+//  keep 5 CTAs per SM: 128 x 11 = 1408 outputs per sub-tile, 2048-element
+//  rings, 512-element chunks (best of the shapes measured on GB300).
+using PairsCfg = TileCfg<128, 11, 11, 9>;
+//  8-byte keys: the same ring bytes as the key+value merge (two 16 KB rings
+//  of 2048 keys, 4 KB chunks), so the same shape.
+using WideCfg = TileCfg<128, 11, 11, 9>;
+
+template <typename K, bool V>
+struct CfgFor {
+    using type = MergeCfg;
+};
+template <typename K>
+struct CfgFor<K, true> {
+    using type = PairsCfg;
+};
+template <>
+struct CfgFor<int64_t, false> {
+    using type = WideCfg;
+};
+template <>
+struct CfgFor<uint64_t, false> {
+    using type = WideCfg;
+};
+template <>
+struct CfgFor<double, false> {
+    using type = WideCfg;
+};
+
+template <typename K, bool V>
+using SmemFor = TileSmem<typename CfgFor<K, V>::type, V, KeyGeom<K>::E>;
+
+enum KernelKind { kKindPartition = 0, kKindTileMerge = 1, kKindBlockSort = 2, kKindCorank = 3, kNumKinds = 4 };
+
+// ------------------------------------------------------------ device state --
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int resident_merge = 0;  // tile-merge CTAs resident per SM (keys only / with values)
+    int resident_merge_v = 0;
+    uint32_t* err = nullptr;
+    int64_t* corank_slot = nullptr;
+};
+
+// Per-device set-up, once per device (thread-safe): SM count, addresses of
+// the library's device words, shared-memory limits of the kernels.
+om_status device_state(DeviceState** out);
+
+// ----------------------------------------------------------------- tracing --
+
+struct TraceRec {
+    int kind;
+    cudaEvent_t e0, e1;
+};
+
+// With tracing on, takes two events and records the first on `stream`.
+// Returns whether tracing is on.
+bool trace_begin(int kind, cudaStream_t stream, TraceRec* rec);
+// Counts one launch and, when `on`, records the second event and files the
+// record; returns the launch's error (cudaGetLastError).
+cudaError_t trace_end(const TraceRec& rec, bool on, cudaStream_t stream);
+
+// Launches through `launch` (a callable issuing exactly one kernel), counting
+// it and, with tracing on, bracketing it with events on `stream`.
+template <typename F>
+cudaError_t traced(int kind, cudaStream_t stream, F&& launch) {
+    TraceRec rec{kind, nullptr, nullptr};
+    const bool on = trace_begin(kind, stream, &rec);
+    launch();
+    return trace_end(rec, on, stream);
+}
+
+// ------------------------------------------------------------------ helpers --
+
+inline bool misaligned(const void* p, int bytes) {
+    return (reinterpret_cast<uintptr_t>(p) & (uintptr_t)(bytes - 1)) != 0;
+}
+inline bool misaligned4(const void* p) { return misaligned(p, 4); }
+
+// Whether [a, a + na elements) and [b, b + nb elements) share a byte.
+inline bool overlaps(const void* a, int64_t na, const void* b, int64_t nb, int elem = 4) {
+    if (na <= 0 || nb <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), a1 = a0 + (uintptr_t)na * (uintptr_t)elem;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + (uintptr_t)nb * (uintptr_t)elem;
+    return a0 < b1 && b0 < a1;
+}
+
+inline om_status cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocation ? OM_ENOMEM : OM_ECUDA; }
+
+// Sub-tiles per CTA output range (see its definition).
+int64_t subtiles_per_range(int64_t subtiles, int64_t resident_ctas);
+
+// Partition + tile-merge launches for one geometry (split has nranges + 1
+// slots of scratch).
+template <typename K, bool V, bool DESC = false>
+cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const DeviceState* d, cudaStream_t st) {
+    using Cfg = typename CfgFor<K, V>::type;
+    using Smem = SmemFor<K, V>;
+    const unsigned pgrid = (unsigned)((g.nranges + 3) / 4);  // one warp per range
+    cudaError_t e =
+        traced(kKindPartition, st, [&] { partition_kernel<K, V, DESC><<<pgrid, 128, 0, st>>>(g, split); });
+    if (e != cudaSuccess) return e;
+    return traced(kKindTileMerge, st, [&] {
+        tile_merge_kernel<Cfg, K, V, DESC><<<(unsigned)g.nranges, Cfg::THREADS, Smem::total, st>>>(g, split, d->err);
+    });
+}
+
+// One merge of A[0..m) and B[0..n) into C (values optional): splitter
+// scratch from the stream-ordered allocator, then partition + tile merge.
+// `resident_per_sm`: tile-merge CTAs of this instantiation resident per SM.
+template <typename K, bool V, bool DESC = false>
+om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, const uint32_t* bv, int64_t n, K* ck,
+                     uint32_t* cv, int resident_per_sm, cudaStream_t st) {
+    DeviceState* d = nullptr;
+    om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    using Cfg = typename CfgFor<K, V>::type;
+    const int64_t total = m + n;
+    const int64_t subtiles = (total + Cfg::T - 1) / Cfg::T;
+    const int64_t resident = (int64_t)d->sm_count * (resident_per_sm > 0 ? resident_per_sm : 1);
+    const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
+    const int64_t nranges = (total + range_len - 1) / range_len;
+    if (nranges > 0x7fffffff) return OM_ERANGE;
+    MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
+    int64_t* split = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&split), (size_t)(nranges + 1) * 8, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return OM_ENOMEM;
+    }
+    e = launch_merge<K, V, DESC>(g, split, d, st);
+    cudaError_t ef = cudaFreeAsync(split, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ef == cudaSuccess ? OM_OK : OM_ECUDA;
+}
+
+}  // namespace om

@@ -44,6 +44,50 @@
 
 namespace om {
 
+// Element size of a key type: E bytes, G = 16 / E elements per 16-byte group
+// (the unit of every bulk copy's start, length and destination).
+template <typename K>
+struct KeyGeom {
+    static constexpr int E = (int)sizeof(K);
+    static constexpr int G = 16 / E;
+    static_assert(E == 4 || E == 8, "keys of 4 or 8 bytes");
+};
+
+// Compare form of a key.  Integers and floats compare as themselves.  A
+// double compares through an int64 with the same order, so the compares run
+// on the integer pipes instead of the FP64 unit (a small fraction of the
+// FP32 rate on this GPU): the sign-magnitude bits become two's complement,
+// which maps -0.0 and +0.0 to the same integer 0 and orders every other
+// non-NaN value as IEEE does.  Outputs keep the original bits.
+template <typename K>
+struct OrderKey {
+    __device__ __forceinline__ static K of(K x) { return x; }
+};
+template <>
+struct OrderKey<double> {
+    // s = 0 (sign clear) or -1 (set): (b ^ (s & 0x7FF..F)) - s is b for a
+    // non-negative value and -(b & 0x7FF..F) for a negative one.
+    __device__ __forceinline__ static long long of(double x) {
+        const long long b = __double_as_longlong(x);
+        const long long s = b >> 63;
+        return (b ^ (s & 0x7FFFFFFFFFFFFFFFLL)) - s;
+    }
+};
+
+// The merge order on compare forms: x (from A) goes out no later than y
+// (from B).  Ascending: x <= y; descending: x >= y.  Either way equal keys
+// take A first, so the merge is stable.
+template <bool DESC, typename O>
+__device__ __forceinline__ bool ord_first(O x, O y) {
+    return DESC ? (y <= x) : (x <= y);
+}
+
+// The same order on keys: a of A goes out no later than b of B.
+template <bool DESC, typename K>
+__device__ __forceinline__ bool a_first(K a, K b) {
+    return ord_first<DESC>(OrderKey<K>::of(a), OrderKey<K>::of(b));
+}
+
 // ---------------------------------------------------------------- geometry --
 
 // A merge problem cut into output ranges of `range_len` outputs.
@@ -117,14 +161,14 @@ __device__ __forceinline__ Segment<K> segment_of(const MergeGeom<K>& g, int64_t 
 // co_rank(k) over global memory: the largest i in [max(0,k-n), min(k,m)]
 // such that i is the lower bound or A[i-1] <= B[k-i].  At most
 // ceil(log2(min(k,m) - max(0,k-n) + 1)) dependent loads.
-template <typename K>
+template <typename K, bool DESC = false>
 __device__ __forceinline__ int64_t corank_global(int64_t k, const K* __restrict__ A, int64_t m,
                                                  const K* __restrict__ B, int64_t n) {
     int64_t lo = k - n > 0 ? k - n : 0;
     int64_t hi = k < m ? k : m;
     while (lo < hi) {
         const int64_t mid = (lo + hi + 1) >> 1;  // lo < mid <= hi
-        if (__ldg(A + mid - 1) <= __ldg(B + k - mid)) {
+        if (a_first<DESC>(__ldg(A + mid - 1), __ldg(B + k - mid))) {
             lo = mid;
         } else {
             hi = mid - 1;
@@ -143,7 +187,7 @@ __device__ __forceinline__ int64_t corank_global(int64_t k, const K* __restrict_
 // dependent loads.  Every lane returns the result.  On unsorted input the
 // passing probes need not form a prefix; the interval still shrinks every
 // round, so the loop always ends.
-template <typename K>
+template <typename K, bool DESC = false>
 __device__ __forceinline__ int64_t corank_warp(int64_t k, const K* __restrict__ A, int64_t m,
                                                const K* __restrict__ B, int64_t n, int lane) {
     int64_t lo = k - n > 0 ? k - n : 0;
@@ -151,7 +195,7 @@ __device__ __forceinline__ int64_t corank_warp(int64_t k, const K* __restrict__ 
     while (hi - lo > 32) {
         const int64_t span = hi - lo;
         const int64_t c = lo + (span * (lane + 1)) / 33;  // lo < c < hi
-        const bool pass = __ldg(A + c - 1) <= __ldg(B + k - c);
+        const bool pass = a_first<DESC>(__ldg(A + c - 1), __ldg(B + k - c));
         const int t = __popc(__ballot_sync(0xffffffffu, pass));
         const int64_t new_lo = (t == 0) ? lo : lo + (span * t) / 33;
         const int64_t new_hi = (t == 32) ? hi : lo + (span * (t + 1)) / 33 - 1;
@@ -160,13 +204,13 @@ __device__ __forceinline__ int64_t corank_warp(int64_t k, const K* __restrict__ 
     }
     const int64_t c = lo + 1 + lane;
     bool pass = false;
-    if (c <= hi) pass = __ldg(A + c - 1) <= __ldg(B + k - c);
+    if (c <= hi) pass = a_first<DESC>(__ldg(A + c - 1), __ldg(B + k - c));
     return lo + __popc(__ballot_sync(0xffffffffu, pass));
 }
 
 // Partition kernel: split[r] = co-rank of the first output of range r within
 // its segment.  One warp per range.
-template <typename K, bool V>
+template <typename K, bool V, bool DESC = false>
 __global__ void __launch_bounds__(128) partition_kernel(MergeGeom<K> g, int64_t* __restrict__ split) {
     const int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -177,20 +221,20 @@ __global__ void __launch_bounds__(128) partition_kernel(MergeGeom<K> g, int64_t*
     const int64_t len = s.m + s.n;
     int64_t k = local * g.range_len;
     if (k > len) k = len;
-    const int64_t i = corank_warp(k, s.ak, s.m, s.bk, s.n, lane);
+    const int64_t i = corank_warp<K, DESC>(k, s.ak, s.m, s.bk, s.n, lane);
     if (lane == 0) split[r] = i;
 }
 
 // One co-rank by one warp.
-template <typename K>
+template <typename K, bool DESC = false>
 __global__ void __launch_bounds__(32) corank_one_kernel(int64_t k, const K* __restrict__ A, int64_t m,
                                                         const K* __restrict__ B, int64_t n, int64_t* out) {
-    const int64_t i = corank_warp(k, A, m, B, n, threadIdx.x & 31);
+    const int64_t i = corank_warp<K, DESC>(k, A, m, B, n, threadIdx.x & 31);
     if (threadIdx.x == 0) *out = i;
 }
 
 // Batched co-rank of one merge (device ks -> device i).
-template <typename K>
+template <typename K, bool DESC = false>
 __global__ void __launch_bounds__(128) corank_batch_kernel(const int64_t* __restrict__ ks, int64_t count,
                                                            const K* __restrict__ A, int64_t m,
                                                            const K* __restrict__ B, int64_t n,
@@ -199,7 +243,7 @@ __global__ void __launch_bounds__(128) corank_batch_kernel(const int64_t* __rest
     if (t >= count) return;
     int64_t k = ks[t];
     k = k < 0 ? 0 : (k > m + n ? m + n : k);
-    out[t] = corank_global(k, A, m, B, n);
+    out[t] = corank_global<K, DESC>(k, A, m, B, n);
 }
 
 // ------------------------------------------------------------ tile merge --
@@ -230,8 +274,9 @@ struct TileCfg {
 };
 
 // Streaming state of one input side (A or B) of one CTA's output range.
-// Positions are in "u" units: u = element index + (address / 4) mod 4 of
-// the side's first element, so u % 4 == 0 exactly at 16-byte boundaries.
+// Positions are in "u" units: u = element index + (address / E) mod G of
+// the side's first element (E-byte keys, G = 16 / E), so u % G == 0 exactly
+// at 16-byte boundaries.
 struct SideStream {
     const char* base16;       // 16-byte aligned address of u = 0 (keys)
     const char* vbase16;      // same for values
@@ -244,17 +289,18 @@ struct SideStream {
     int next_wait;            // next chunk (relative to c_first) not yet waited for
 };
 
-template <typename Cfg>
+template <typename Cfg, typename K>
 __device__ __forceinline__ void side_init(SideStream& s, const void* keys, const void* vals, int64_t len,
                                           int64_t lo, int64_t hi) {
+    constexpr int E = KeyGeom<K>::E, G = KeyGeom<K>::G;
     const uintptr_t a = reinterpret_cast<uintptr_t>(keys);
-    const int64_t mis = (int64_t)((a >> 2) & 3);
+    const int64_t mis = (int64_t)((a / E) & (G - 1));
     s.base16 = reinterpret_cast<const char*>(a & ~uintptr_t(15));
     s.vbase16 = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(vals) & ~uintptr_t(15));
     s.arr_lo = mis;
     s.arr_hi = mis + len;
-    s.arr_lo4 = (s.arr_lo + 3) & ~int64_t(3);
-    s.arr_hi4 = s.arr_hi & ~int64_t(3);
+    s.arr_lo4 = (s.arr_lo + G - 1) & ~int64_t(G - 1);
+    s.arr_hi4 = s.arr_hi & ~int64_t(G - 1);
     s.u_lo = mis + lo;
     s.u_hi = mis + hi;
     s.head = s.u_lo;
@@ -267,28 +313,31 @@ __device__ __forceinline__ void side_init(SideStream& s, const void* keys, const
 // Thread 0 only: request chunk c of side s into its ring slots.  A chunk
 // that lies wholly inside the CTA's part and the array's aligned interior is
 // one bulk copy per array.  Otherwise the 16-byte aligned body goes through
-// a bulk copy and the at most 3 + 3 elements at the two ends of the side
-// array that do not fill a 16-byte group are loaded with plain loads; those
+// a bulk copy and the at most (G - 1) + (G - 1) elements at the two ends of
+// the side array that do not fill a 16-byte group are loaded with plain
+// loads; those
 // stores are published to the other threads by the barrier's arrive
 // (release) and their wait (acquire).
 template <typename Cfg, typename K, bool V>
 __device__ __forceinline__ void issue_chunk(SideStream& s, int64_t c, K* ring_k, uint32_t* ring_v,
                                             uint64_t* bars, uint64_t policy) {
+    constexpr int E = KeyGeom<K>::E, G = KeyGeom<K>::G;
+    static_assert(!V || E == 4, "values are 32-bit and share the keys' u positions");
     const int64_t cs = c << Cfg::CH_LOG2;
     const int64_t ce = cs + Cfg::CH;
     uint64_t* bar = &bars[(int)(c - s.c_first) & (Cfg::NCH - 1)];
     if (cs >= s.u_lo && ce <= s.u_hi && cs >= s.arr_lo4 && ce <= s.arr_hi4) {
         const uint32_t slot = (uint32_t)cs & Cfg::RMASK;
-        mbar_arrive_expect_tx(bar, (uint32_t)Cfg::CH * 4u * (V ? 2u : 1u));
-        bulk_copy_g2s(ring_k + slot, s.base16 + 4 * cs, Cfg::CH * 4, bar, policy);
+        mbar_arrive_expect_tx(bar, (uint32_t)Cfg::CH * (uint32_t)E * (V ? 2u : 1u));
+        bulk_copy_g2s(ring_k + slot, s.base16 + E * cs, Cfg::CH * E, bar, policy);
         if (V) bulk_copy_g2s(ring_v + slot, s.vbase16 + 4 * cs, Cfg::CH * 4, bar, policy);
         return;
     }
     const int64_t s0 = cs > s.u_lo ? cs : s.u_lo;
     const int64_t e0 = ce < s.u_hi ? ce : s.u_hi;
-    int64_t bs = s0 & ~int64_t(3);
+    int64_t bs = s0 & ~int64_t(G - 1);
     if (bs < s.arr_lo4) bs = s.arr_lo4;
-    int64_t be = (e0 + 3) & ~int64_t(3);
+    int64_t be = (e0 + G - 1) & ~int64_t(G - 1);
     if (be > s.arr_hi4) be = s.arr_hi4;
     const K* gk = reinterpret_cast<const K*>(s.base16);
     const uint32_t* gv = reinterpret_cast<const uint32_t*>(s.vbase16);
@@ -298,7 +347,7 @@ __device__ __forceinline__ void issue_chunk(SideStream& s, int64_t c, K* ring_k,
     if (be > bs) {
         p1 = bs;
         q0 = be;
-        bytes = (uint32_t)(be - bs) * 4u;
+        bytes = (uint32_t)(be - bs) * (uint32_t)E;
     }
     for (int64_t u = p0; u < p1; ++u) {
         ring_k[(uint32_t)u & Cfg::RMASK] = gk[u];
@@ -314,7 +363,7 @@ __device__ __forceinline__ void issue_chunk(SideStream& s, int64_t c, K* ring_k,
     mbar_arrive_expect_tx(bar, V ? 2 * bytes : bytes);
     if (bytes) {
         const uint32_t slot = (uint32_t)bs & Cfg::RMASK;
-        bulk_copy_g2s(ring_k + slot, s.base16 + 4 * bs, bytes, bar, policy);
+        bulk_copy_g2s(ring_k + slot, s.base16 + E * bs, bytes, bar, policy);
         if (V) bulk_copy_g2s(ring_v + slot, s.vbase16 + 4 * bs, bytes, bar, policy);
     }
 }
@@ -346,9 +395,10 @@ __device__ __forceinline__ bool wait_window(SideStream& s, int64_t need_end, uin
 
 // co_rank(d) of the two ring windows, A = ring[(ha + x) & mask] and
 // B = ring[RING | ((hb + x) & mask)]: the largest i in [lo, hi] with i == lo
-// or A[i-1] <= B[d-i], by a fixed sequence of power-of-two steps (no data
-// dependent trip count, so a warp never diverges on it).
-template <typename Cfg, typename K>
+// or A[i-1] <= B[d-i] (in the merge order), by a fixed sequence of
+// power-of-two steps (no data dependent trip count, so a warp never diverges
+// on it).
+template <typename Cfg, typename K, bool DESC = false>
 __device__ __forceinline__ int corank_ring(int d, int lo, int hi, const K* ring, uint32_t ha, uint32_t hb) {
 #pragma unroll
     for (int step = Cfg::SEARCH_TOP; step > 0; step >>= 1) {
@@ -356,7 +406,7 @@ __device__ __forceinline__ int corank_ring(int d, int lo, int hi, const K* ring,
         if (cand <= hi) {
             const K x = ring[(ha + (uint32_t)(cand - 1)) & Cfg::RMASK];
             const K y = ring[Cfg::RING | ((hb + (uint32_t)(d - cand)) & Cfg::RMASK)];
-            if (x <= y) lo = cand;
+            if (a_first<DESC>(x, y)) lo = cand;
         }
     }
     return lo;
@@ -367,7 +417,7 @@ __device__ __forceinline__ int corank_ring(int d, int lo, int hi, const K* ring,
 // (ties go to A).  GUARD adds the exhaustion tests needed when a window ends
 // before the sub-tile does (the last sub-tile of a range); without GUARD all
 // VT steps run.  Returns the A position after the last step.
-template <typename Cfg, typename K, bool V, bool GUARD>
+template <typename Cfg, typename K, bool V, bool GUARD, bool DESC = false>
 __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, int wb, const K* ring,
                                                  const uint32_t* vring, uint32_t ha, uint32_t hb, K (&keys)[Cfg::VT],
                                                  uint32_t (&vals)[Cfg::VT]) {
@@ -379,6 +429,9 @@ __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, 
     const uint32_t ia = ai & M, ib = Cfg::RING | (bi & M);
     K ak = ring[ia];
     K bk = ring[ib];
+    // compare forms of the two heads, each computed once when its key is read
+    auto ao = OrderKey<K>::of(ak);
+    auto bo = OrderKey<K>::of(bk);
     uint32_t av = 0, bv = 0;
     if (V) {
         av = vring[ia];
@@ -387,7 +440,7 @@ __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, 
 #pragma unroll
     for (int v = 0; v < Cfg::VT; ++v) {
         if (!GUARD || v < cnt) {
-            const bool p = GUARD ? ((bi >= b_end) || ((ai < a_end) && (ak <= bk))) : (ak <= bk);
+            const bool p = GUARD ? ((bi >= b_end) || ((ai < a_end) && ord_first<DESC>(ao, bo))) : ord_first<DESC>(ao, bo);
             keys[v] = p ? ak : bk;
             if (V) vals[v] = p ? av : bv;
             ai += p ? 1u : 0u;
@@ -395,8 +448,11 @@ __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, 
             if (v + 1 < Cfg::VT) {
                 const uint32_t idx = p ? (ai & M) : (Cfg::RING | (bi & M));
                 const K nk = ring[idx];
+                const auto no = OrderKey<K>::of(nk);
                 ak = p ? nk : ak;
                 bk = p ? bk : nk;
+                ao = p ? no : ao;
+                bo = p ? bo : no;
                 if (V) {
                     const uint32_t nv = vring[idx];
                     av = p ? nv : av;
@@ -416,13 +472,12 @@ constexpr int kPartialMargin = 128;
 // (A ring, then B ring, so one masked index addresses either), values
 // likewise, the output stage, the chunk barriers of both sides, the
 // producer/consumer barriers and the per-sub-tile window descriptors.
-template <typename Cfg, bool V>
+template <typename Cfg, bool V, int E = 4>
 struct TileSmem {
-    static constexpr size_t ring_bytes = (size_t)2 * Cfg::RING * 4 * (V ? 2 : 1);
-    static constexpr size_t stage_bytes = (size_t)Cfg::STAGE * 4 * (V ? 2 : 1);
+    static constexpr size_t ring_bytes = (size_t)2 * Cfg::RING * (E + (V ? 4 : 0));
+    static constexpr size_t stage_bytes = (size_t)Cfg::STAGE * (E + (V ? 4 : 0));
     // chunk barriers of A and B, ready[2], done[2], stage_free
     static constexpr size_t bar_bytes = (size_t)(2 * Cfg::NCH + 5) * 8;
-    // window descriptors: 2 x {ha, hb, wa, wb, teff, pad...} ints, a_used[2], abort
     // window descriptors: 2 x {ha, hb, wa, wb, teff, partial_a, partial_b, -},
     // a_used[2], redo[2], abort, padding
     static constexpr size_t info_bytes = 2 * 8 * 4 + 8 * 4;
@@ -442,14 +497,15 @@ struct TileSmem {
 //   consumers: wait ready[s] -> co-rank + serial merge -> wait stage_free
 //             (s-1) -> write the stage -> arrive done[s]
 // Consumers never run a CTA-wide barrier and keep no streaming state.
-template <typename Cfg, typename K, bool V>
+template <typename Cfg, typename K, bool V, bool DESC = false>
 __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g,
                                                                     const int64_t* __restrict__ split,
                                                                     uint32_t* err) {
     constexpr int NT = Cfg::NT;
     constexpr int VT = Cfg::VT;
     constexpr int T = Cfg::T;
-    using Smem = TileSmem<Cfg, V>;
+    constexpr int E = KeyGeom<K>::E, G = KeyGeom<K>::G;
+    using Smem = TileSmem<Cfg, V, E>;
 
     extern __shared__ __align__(128) unsigned char smem[];
     K* ring = reinterpret_cast<K*>(smem);
@@ -483,7 +539,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         return;  // whole CTA
     }
     const uintptr_t caddr = reinterpret_cast<uintptr_t>(s.ck);
-    const int misc = (int)((caddr >> 2) & 3);
+    const int misc = (int)((caddr / E) & (G - 1));
 
     if (tid == 0) {
         for (int c = 0; c < Cfg::NCH; ++c) {
@@ -509,9 +565,9 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         const bool side_a = tid == NT;
         SideStream S;
         if (side_a) {
-            side_init<Cfg>(S, s.ak, s.av, s.m, i0, i1);
+            side_init<Cfg, K>(S, s.ak, s.av, s.m, i0, i1);
         } else {
-            side_init<Cfg>(S, s.bk, s.bv, s.n, j0, j1);
+            side_init<Cfg, K>(S, s.bk, s.bv, s.n, j0, j1);
         }
         K* rk = side_a ? ring : ring + Cfg::RING;
         uint32_t* rv = V ? (side_a ? vring : vring + Cfg::RING) : nullptr;
@@ -568,7 +624,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
                 bool ok2 = mbar_wait_bounded(&ready[it & 1], (uint32_t)(it >> 1) & 1u, err);
                 if (ok2 && (inf[5] | inf[6])) {
                     const int wa_ = inf[2], wb_ = inf[3];
-                    const int r = corank_ring<Cfg, K>(teff, teff - wb_ > 0 ? teff - wb_ : 0, teff < wa_ ? teff : wa_,
+                    const int r = corank_ring<Cfg, K, DESC>(teff, teff - wb_ > 0 ? teff - wb_ : 0, teff < wa_ ? teff : wa_,
                                                       ring, (uint32_t)inf[0], (uint32_t)inf[1]);
                     a_used_slot[it & 1] = r;
                     redo = (r < wa_ && teff - r < wb_) ? 0 : 1;
@@ -593,14 +649,14 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
             first_new = S.next_issue;
             refill<Cfg, K, V>(S, rk, rv, bars, policy);
             if (side_a) {
-                // C[kdone, kdone + teff) <- stage.  u = misc + k; stage slot = u - (u0 & ~3).
+                // C[kdone, kdone + teff) <- stage.  u = misc + k; stage slot = u - (u0 & ~(G-1)).
                 const int64_t cu0 = misc + kdone, cu1 = cu0 + teff;
-                const int64_t g0 = cu0 & ~int64_t(3);
-                const int64_t bs = (cu0 + 3) & ~int64_t(3);
-                const int64_t be = cu1 & ~int64_t(3);
+                const int64_t g0 = cu0 & ~int64_t(G - 1);
+                const int64_t bs = (cu0 + G - 1) & ~int64_t(G - 1);
+                const int64_t be = cu1 & ~int64_t(G - 1);
                 int64_t p1 = cu1, q0 = cu1;
                 if (be > bs) {
-                    bulk_copy_s2g(cbase16 + 4 * bs, stage_k + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
+                    bulk_copy_s2g(cbase16 + E * bs, stage_k + (bs - g0), (uint32_t)(be - bs) * (uint32_t)E, policy);
                     if (V) bulk_copy_s2g(cvbase16 + 4 * bs, stage_v + (bs - g0), (uint32_t)(be - bs) * 4u, policy);
                     p1 = bs;
                     q0 = be;
@@ -654,8 +710,8 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         int cnt = VT;
         uint32_t apos;
         if (full) {
-            const int a = corank_ring<Cfg, K>(d, 0, d, ring, ha, hb);
-            apos = merge_serial<Cfg, K, V, false>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
+            const int a = corank_ring<Cfg, K, DESC>(d, 0, d, ring, ha, hb);
+            apos = merge_serial<Cfg, K, V, false, DESC>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
         } else if (partial) {
             // Windows cut to the data that has landed (teff == T).  Searches
             // stay inside them and the merge runs without exhaustion tests;
@@ -663,14 +719,14 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
             // the sub-tile is discarded and published again with whole windows.
             const int lo = d - wb > 0 ? d - wb : 0;
             const int hi = d < wa ? d : wa;
-            const int a = corank_ring<Cfg, K>(d, lo, hi, ring, ha, hb);
-            apos = merge_serial<Cfg, K, V, false>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
+            const int a = corank_ring<Cfg, K, DESC>(d, lo, hi, ring, ha, hb);
+            apos = merge_serial<Cfg, K, V, false, DESC>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
         } else {
             cnt = (teff - d < VT) ? teff - d : VT;
             const int lo = d - wb > 0 ? d - wb : 0;
             const int hi = d < wa ? d : wa;
-            const int a = corank_ring<Cfg, K>(d, lo, hi, ring, ha, hb);
-            apos = merge_serial<Cfg, K, V, true>(a, d - a, cnt, wa, wb, ring, vring, ha, hb, keys, vals);
+            const int a = corank_ring<Cfg, K, DESC>(d, lo, hi, ring, ha, hb);
+            apos = merge_serial<Cfg, K, V, true, DESC>(a, d - a, cnt, wa, wb, ring, vring, ha, hb, keys, vals);
         }
         if (it > 0 && !mbar_wait_bounded(stage_free, (uint32_t)(it - 1) & 1u, err)) {
             *abort_flag = 1;

@@ -79,3 +79,25 @@ def test_host_argument_checks():
     # co-rank with one side empty is forced and needs no device
     assert L.om_corank_i32(3, None, 0, 0x2000, 5) == 0
     assert L.om_corank_i32(3, 0x1000, 5, None, 0) == 3
+
+
+def test_merge_keys_host_argument_checks():
+    """om_merge_keys: unknown type or order, alignment to the key size and
+    overlap in key-size units are rejected on the host."""
+    import ordered_merge_gb300 as om
+
+    L = om.lib()
+    i64, f32 = om.KEY_TYPES["i64"][0], om.KEY_TYPES["f32"][0]
+    assert L.om_merge_keys(6, 0, 0x1000, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+    assert L.om_merge_keys(-1, 0, 0x1000, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+    assert L.om_merge_keys(f32, 2, 0x1000, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+    assert L.om_merge_keys(f32, 0, None, 0, None, 0, None, None) == om.OM_OK
+    assert L.om_merge_keys(f32, 0, None, -1, None, 0, None, None) == om.OM_EINVAL
+    assert L.om_merge_keys(f32, 0, 0x1000, 2**62, 0x2000, 2**62, 0x3000, None) == om.OM_ERANGE
+    # 8-byte keys need 8-byte alignment; 4 is not enough
+    assert L.om_merge_keys(i64, 0, 0x1004, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+    assert L.om_merge_keys(i64, 1, 0x1000, 4, 0x2000, 4, 0x300C, None) == om.OM_EINVAL
+    assert L.om_merge_keys(f32, 0, 0x1002, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+    # overlap counts 8 bytes per element: C = [0x2000, 0x2040) meets B at 0x2020
+    assert L.om_merge_keys(i64, 0, 0x1000, 4, 0x2020, 4, 0x2000, None) == om.OM_EINVAL
+    assert L.om_merge_keys(i64, 0, None, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL

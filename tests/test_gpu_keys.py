@@ -1,0 +1,193 @@
+"""GPU parity of om_merge_keys (six key types, ascending and descending)
+against the CPU oracle: element by element, bit for bit, with guard bands
+around every output.
+
+Sizes span one sub-tile, many sub-tiles and output ranges, and ragged
+tails; edge cases cover empty and one-element sides, heavy ties, -0.0 and
++0.0 (equal keys with different bits, so the tie rule is visible), the
+types' extreme values, infinities and subnormals, and pointers that are not
+16-byte aligned.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TYPES = ["i32", "u32", "f32", "i64", "u64", "f64"]
+NP = {"i32": np.int32, "u32": np.uint32, "f32": np.float32, "i64": np.int64, "u64": np.uint64, "f64": np.float64}
+GUARD = 36
+
+
+def _carrier(name):
+    """The signed integer numpy/torch types that carry a key type's bits."""
+    return (np.int32, torch.int32) if np.dtype(NP[name]).itemsize == 4 else (np.int64, torch.int64)
+
+
+def to_dev(x, name, offset=0):
+    """Device copy of x whose first element sits `offset` elements past a
+    16-byte boundary."""
+    npc, tc = _carrier(name)
+    h = torch.from_numpy(np.ascontiguousarray(x, dtype=NP[name]).view(npc))
+    buf = torch.empty(h.numel() + 4, dtype=tc, device="cuda")
+    view = buf[offset: offset + h.numel()]
+    view.copy_(h)
+    return view
+
+
+def run(om, name, A, B, desc=False, offs=(0, 0, 0)):
+    npc, tc = _carrier(name)
+    total = A.size + B.size
+    dA, dB = to_dev(A, name, offs[0]), to_dev(B, name, offs[1])
+    sentinel = -0x5A5A5A5B
+    buf = torch.full((total + 2 * GUARD + 4,), sentinel, dtype=tc, device="cuda")
+    C = buf[GUARD + offs[2]: GUARD + offs[2] + total]
+    om.merge_keys(dA, dB, C, key_type=name, descending=desc)
+    torch.cuda.synchronize()
+    assert om.device_error() == 0
+    h = buf.cpu().numpy()
+    assert np.all(h[: GUARD + offs[2]] == sentinel) and np.all(h[GUARD + offs[2] + total:] == sentinel), \
+        "merge wrote outside C"
+    return C.cpu().numpy().view(NP[name])
+
+
+def check(om, name, A, B, desc=False, offs=(0, 0, 0)):
+    A = np.ascontiguousarray(A, dtype=NP[name])
+    B = np.ascontiguousarray(B, dtype=NP[name])
+    got = run(om, name, A, B, desc, offs)
+    want = oracle.merge_keys(A, B, descending=desc)
+    npc, _ = _carrier(name)
+    g, w = got.view(npc), want.view(npc)
+    if not np.array_equal(g, w):
+        bad = int(np.flatnonzero(g != w)[0])
+        raise AssertionError(f"{name} desc={desc}: first mismatch at {bad}: got {got[bad]!r}, want {want[bad]!r} "
+                             f"(m={A.size}, n={B.size}, offs={offs})")
+
+
+def sorted_keys(rng, name, size, span, desc):
+    """`size` sorted keys of type `name` drawn from about `span` distinct
+    values (heavy ties for a small span); floats include signed zeros."""
+    dt = NP[name]
+    if np.issubdtype(dt, np.floating):
+        base = rng.integers(-span, span, size).astype(np.float64) / 4.0
+        base[rng.random(size) < 0.05] = 0.0
+        x = base.astype(dt)
+        x[(x == 0) & (rng.random(size) < 0.5)] = -0.0
+    elif np.issubdtype(dt, np.unsignedinteger):
+        info = np.iinfo(dt)
+        if span >= 1 << 20:
+            x = rng.integers(0, info.max, size, dtype=dt, endpoint=True)
+        else:
+            x = (rng.integers(0, span, size, dtype=np.int64).astype(dt) * dt(info.max // max(span, 1)))
+    else:
+        info = np.iinfo(dt)
+        if span >= 1 << 20:
+            x = rng.integers(info.min, info.max, size, dtype=dt, endpoint=True)
+        else:
+            x = rng.integers(-span, span, size, dtype=np.int64).astype(dt)
+    x = np.sort(x, kind="stable")
+    return x[::-1].copy() if desc else x
+
+
+@pytest.mark.parametrize("desc", [False, True], ids=["asc", "desc"])
+@pytest.mark.parametrize("name", TYPES)
+@pytest.mark.parametrize("m,n", [(0, 0), (0, 7), (7, 0), (1, 1), (1407, 1), (1408, 1408), (2944, 1),
+                                 (12345, 54321), (250001, 249999)])
+def test_shapes(gpu, name, desc, m, n):
+    rng = np.random.default_rng(m * 31 + n + 7 * TYPES.index(name) + desc)
+    for span in (8, 1 << 30):
+        check(gpu, name, sorted_keys(rng, name, m, span, desc), sorted_keys(rng, name, n, span, desc), desc)
+
+
+@pytest.mark.parametrize("desc", [False, True], ids=["asc", "desc"])
+@pytest.mark.parametrize("name", TYPES)
+def test_extremes(gpu, name, desc):
+    dt = NP[name]
+    if np.issubdtype(dt, np.floating):
+        vals = [-np.inf, -np.finfo(dt).max, -1.0, -np.finfo(dt).tiny, -0.0, 0.0, np.finfo(dt).smallest_subnormal,
+                1.0, np.finfo(dt).max, np.inf]
+    else:
+        info = np.iinfo(dt)
+        vals = sorted({int(info.min), int(info.min) + 1, -1 if info.min < 0 else 1, 0, 1 << 7,
+                       int(info.max) // 2, int(info.max) // 2 + 1, int(info.max) - 1, int(info.max)})
+    rng = np.random.default_rng(TYPES.index(name) * 2 + desc)
+    src = np.array(vals, dtype=dt)
+    for m, n in [(len(vals), len(vals)), (30011, 20011)]:
+        A = np.sort(src[rng.integers(0, src.size, m)], kind="stable")
+        B = np.sort(src[rng.integers(0, src.size, n)], kind="stable")
+        if desc:
+            A, B = A[::-1].copy(), B[::-1].copy()
+        check(gpu, name, A, B, desc)
+
+
+@pytest.mark.parametrize("name", ["f32", "f64"])
+def test_signed_zero_ties(gpu, name):
+    """All keys zero: A holds -0.0 and B +0.0 (then the reverse); the output
+    must be all of A's zeros, then all of B's, in either order."""
+    dt = NP[name]
+    for desc in (False, True):
+        for za, zb in ((-0.0, 0.0), (0.0, -0.0)):
+            check(gpu, name, np.full(40007, za, dt), np.full(30011, zb, dt), desc)
+
+
+@pytest.mark.parametrize("name", TYPES)
+@pytest.mark.parametrize("offs", [(1, 0, 0), (0, 1, 1), (1, 1, 0), (3, 2, 1)])
+def test_misaligned_pointers(gpu, name, offs):
+    if np.dtype(NP[name]).itemsize == 8:
+        offs = tuple(o & 1 for o in offs)  # one 8-byte element = half a 16-byte group
+    rng = np.random.default_rng(sum(offs) + TYPES.index(name))
+    for desc in (False, True):
+        check(gpu, name, sorted_keys(rng, name, 54321, 500, desc), sorted_keys(rng, name, 43210, 500, desc),
+              desc, offs)
+        check(gpu, name, sorted_keys(rng, name, 13, 5, desc), sorted_keys(rng, name, 1, 5, desc), desc, offs)
+
+
+@pytest.mark.parametrize("name,desc", [("i64", False), ("f64", True), ("u32", True), ("f32", False)])
+@pytest.mark.parametrize("per_range", [8, 40])
+def test_long_ranges_uneven_consumption(gpu, monkeypatch, name, desc, per_range):
+    """Many sub-tiles per output range, with stretches where one side supplies
+    every output: windows cut to landed data, and sub-tiles merged again with
+    whole windows."""
+    monkeypatch.setenv("OM_SUBTILES_PER_RANGE", str(per_range))
+    rng = np.random.default_rng(per_range + TYPES.index(name))
+    labels = []
+    for q in range(300):
+        if q % 6 == 2:
+            labels += [q % 2] * int(rng.integers(2000, 7000))
+        else:
+            labels += list(rng.integers(0, 2, int(rng.integers(1000, 5000))))
+    labels = np.array(labels)
+    keys = (np.arange(labels.size, dtype=np.int64) // 3 - labels.size // 6)
+    if NP[name] in (np.uint32, np.uint64):
+        keys = keys - keys.min()
+    keys = keys.astype(NP[name])
+    if desc:
+        keys = keys[::-1].copy()
+        labels = labels[::-1].copy()
+    A, B = keys[labels == 0], keys[labels == 1]
+    check(gpu, name, A, B, desc)
+    check(gpu, name, B, A, desc)
+
+
+@pytest.mark.parametrize("name", ["i32", "f32"])
+def test_i32_ascending_matches_merge_i32(gpu, name):
+    """The typed call with i32 ascending keys gives om_merge_i32's output."""
+    rng = np.random.default_rng(3)
+    A = sorted_keys(rng, "i32", 100003, 1000, False)
+    B = sorted_keys(rng, "i32", 99997, 1000, False)
+    dA, dB = to_dev(A, "i32"), to_dev(B, "i32")
+    c1 = gpu.merge_i32(dA, dB)
+    c2 = gpu.merge_keys(dA, dB, key_type="i32")
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+
+
+@pytest.mark.parametrize("name", ["i64", "f64", "u64"])
+def test_wide_keys_large(gpu, name):
+    """2^24 outputs of 8-byte keys: many ranges per CTA wave; checked in full."""
+    rng = np.random.default_rng(11)
+    for desc in (False, True):
+        check(gpu, name, sorted_keys(rng, name, (1 << 23) + 3, 1 << 30, desc),
+              sorted_keys(rng, name, (1 << 23) - 3, 1 << 30, desc), desc)
