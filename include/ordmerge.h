@@ -201,6 +201,24 @@ typedef enum {
 om_status om_merge_keys(int key_type, int order, const void *A, int64_t m,
                         const void *B, int64_t n, void *C, void *stream);
 
+/*
+ * Stable sort of keys[0..n) of type `key_type` into `order`, in place,
+ * carrying the uint32 vals along (vals may be NULL).  The pass schedule of
+ * om_merge_sort_u32 with that type's compare: 4096-key tiles sorted in
+ * shared memory, then co-rank-split merge passes ("排序 (Sorting) 練習題",
+ * merge-sort stages).  Equal keys (including -0.0 and +0.0) keep their
+ * input order in either order.
+ *  - keys aligned to the key size.  Values ride only with 4-byte keys
+ *    (I32, U32, F32): vals with an 8-byte key type is OM_EINVAL.  vals, if
+ *    given, has the same address modulo 16 as keys and does not overlap it.
+ *  - Floating-point keys must not hold NaN (unsorted output otherwise; every
+ *    kernel still terminates).
+ *  - Needs n * key size (plus 4 * n with vals) bytes of stream-ordered
+ *    scratch.  Other rules and errors are those of om_merge_sort_u32.
+ */
+om_status om_merge_sort_keys(int key_type, int order, void *keys,
+                             uint32_t *vals, int64_t n, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -64,6 +64,8 @@ def _load():
     lib.om_trace_read.restype = I32
     lib.om_merge_keys.argtypes = [I32, I32, P, I64, P, I64, P, P]
     lib.om_merge_keys.restype = I32
+    lib.om_merge_sort_keys.argtypes = [I32, I32, P, P, I64, P]
+    lib.om_merge_sort_keys.restype = I32
     lib.om_launch_count.argtypes = []
     lib.om_launch_count.restype = ctypes.c_uint64
     return lib
@@ -196,6 +198,25 @@ def om_merge_keys(A, B, C=None, key_type=None, descending=False, stream=None):
     return C
 
 
+def om_merge_sort_keys(keys, vals=None, key_type=None, descending=False, stream=None):
+    """Stable in-place sort of a device tensor of keys (type from its dtype
+    or `key_type`), nondecreasing or (descending) nonincreasing, carrying
+    optional 4-byte values (4-byte keys only)."""
+    name = key_type or _key_type_of(keys.dtype)
+    if name not in KEY_TYPES:
+        raise ValueError(f"unknown key type {name!r}")
+    code, size = KEY_TYPES[name]
+    n = keys.numel()
+    if vals is not None and vals.numel() != n:
+        raise ValueError("vals must have as many elements as keys")
+    _check(
+        _lib.om_merge_sort_keys(code, OM_DESCENDING if descending else OM_ASCENDING, _ptr_sized(keys, "keys", size),
+                                _ptr4(vals, "vals") if vals is not None else None, n, _stream(stream)),
+        "om_merge_sort_keys",
+    )
+    return keys, vals
+
+
 def om_merge_pairs_u32(keysA, valsA, keysB, valsB, keysC=None, valsC=None, stream=None):
     """Stable merge of (uint32 key, uint32 value) pairs; keys compared unsigned.
 
@@ -268,5 +289,6 @@ corank_i32_batch = om_corank_i32_batch
 merge_i32 = om_merge_i32
 merge_pairs_u32 = om_merge_pairs_u32
 merge_keys = om_merge_keys
+merge_sort_keys = om_merge_sort_keys
 merge_sort_u32 = om_merge_sort_u32
 device_error = om_device_error

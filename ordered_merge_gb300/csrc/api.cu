@@ -10,16 +10,8 @@
 #include <cuda_runtime.h>
 
 #include "api_internal.cuh"
-#include "sort_kernels.cuh"
 
 namespace om {
-
-//  sort: one block pass sorts 256 x 16 = 4096-element tiles in shared memory
-//        (runs of 16 in registers, then merges of whole pairs of runs per
-//        CTA through 1024 to 4096); later passes use
-//        the partition + tile-merge kernels on each pair of runs.
-using SmallMergeCfg = BlockSortCfg<256, 16>;
-constexpr int kEarlyTo = SmallMergeCfg::TILE;  // runs after the block pass: 4096
 
 // ------------------------------------------------------------ device state --
 
@@ -51,8 +43,6 @@ om_status device_state(DeviceState** out) {
         e = e ? e : set_smem(tile_merge_kernel<MergeCfg, int32_t, false>, SmemFor<int32_t, false>::total);
         e = e ? e : set_smem(tile_merge_kernel<MergeCfg, uint32_t, false>, SmemFor<uint32_t, false>::total);
         e = e ? e : set_smem(tile_merge_kernel<PairsCfg, uint32_t, true>, SmemFor<uint32_t, true>::total);
-        e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, true>, block_sort_smem_bytes<SmallMergeCfg, true>());
-        e = e ? e : set_smem(block_sort_kernel<SmallMergeCfg, false>, block_sort_smem_bytes<SmallMergeCfg, false>());
         if (e != cudaSuccess) return OM_ECUDA;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.resident_merge,
                                                           tile_merge_kernel<MergeCfg, int32_t, false>,
@@ -151,85 +141,6 @@ int64_t subtiles_per_range(int64_t subtiles, int64_t resident_ctas) {
     return env_int("OM_SUBTILES_PER_RANGE", s);
 }
 
-template <bool V>
-static om_status sort_impl(uint32_t* keys, uint32_t* vals, int64_t n, cudaStream_t st) {
-    DeviceState* d = nullptr;
-    om_status s = device_state(&d);
-    if (s != OM_OK) return s;
-
-    // Pass schedule: one block pass sorts each 4096-element tile in shared
-    // memory (early stages: many small merges per block); then one
-    // co-rank-split late pass per doubling.  `passes` counts the global
-    // passes after the block pass.
-    int passes = 0;
-    for (int64_t r = kEarlyTo; r < n; r *= 2) ++passes;
-    using Cfg = typename CfgFor<uint32_t, V>::type;
-    const int64_t subtiles = (n + Cfg::T - 1) / Cfg::T;
-    const int64_t resident = (int64_t)d->sm_count * (V ? d->resident_merge_v : d->resident_merge);
-    const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
-    // splitter slots for the largest late pass (every pair gets the same
-    // number of ranges, including a short last pair), plus one
-    int64_t max_ranges = 1;
-    for (int64_t r = kEarlyTo; r < n; r *= 2) {
-        const int64_t npairs = (n + 2 * r - 1) / (2 * r);
-        const int64_t rps = (2 * r + range_len - 1) / range_len;
-        if (npairs * rps + 1 > max_ranges) max_ranges = npairs * rps + 1;
-    }
-
-    uint32_t* tk = nullptr;
-    uint32_t* tv = nullptr;
-    int64_t* split = nullptr;
-    cudaError_t e = cudaSuccess;
-    if (passes > 0) {
-        e = cudaMallocAsync(reinterpret_cast<void**>(&tk), (size_t)n * 4, st);
-        if (e == cudaSuccess && V) e = cudaMallocAsync(reinterpret_cast<void**>(&tv), (size_t)n * 4, st);
-        if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&split), (size_t)max_ranges * 8, st);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            if (tk) cudaFreeAsync(tk, st);
-            if (tv) cudaFreeAsync(tv, st);
-            return OM_ENOMEM;
-        }
-    }
-    // The block pass writes where the pass count's parity makes the last
-    // pass land back in keys / vals.
-    uint32_t* src_k = (passes % 2 == 0) ? keys : tk;
-    uint32_t* src_v = (passes % 2 == 0) ? vals : tv;
-    uint32_t* dst_k = (passes % 2 == 0) ? tk : keys;
-    uint32_t* dst_v = (passes % 2 == 0) ? tv : vals;
-
-    {
-        // run sort and early merges in one launch: every CTA sorts 16
-        // elements per thread in registers, then merges runs 16 -> ... ->
-        // 1024 -> ... -> kEarlyTo in shared memory (whole pairs per CTA)
-        const unsigned grid = (unsigned)((n + SmallMergeCfg::TILE - 1) / SmallMergeCfg::TILE);
-        e = traced(kKindBlockSort, st, [&] {
-            block_sort_kernel<SmallMergeCfg, V><<<grid, SmallMergeCfg::NT, block_sort_smem_bytes<SmallMergeCfg, V>(),
-                                                  st>>>(keys, vals, src_k, src_v, n, 1, kEarlyTo);
-        });
-    }
-    for (int64_t r = kEarlyTo; e == cudaSuccess && r < n; r *= 2) {
-        // late pass: co-rank split of each pair of runs into output ranges
-        const int64_t npairs = (n + 2 * r - 1) / (2 * r);
-        const int64_t rps = (2 * r + range_len - 1) / range_len;
-        MergeGeom<uint32_t> g{src_k, src_v, nullptr, nullptr, dst_k, dst_v, n, 0, r, range_len, rps, npairs * rps};
-        if (g.nranges + 1 > max_ranges || g.nranges > 0x7fffffff) {
-            e = cudaErrorInvalidValue;
-            break;
-        }
-        e = launch_merge<uint32_t, V>(g, split, d, st);
-        uint32_t* t;
-        t = src_k; src_k = dst_k; dst_k = t;
-        t = src_v; src_v = dst_v; dst_v = t;
-    }
-    if (passes > 0) {
-        cudaFreeAsync(split, st);
-        cudaFreeAsync(tk, st);
-        if (V) cudaFreeAsync(tv, st);
-    }
-    return e == cudaSuccess ? OM_OK : cuda_fail(e);
-}
-
 }  // namespace om
 
 using namespace om;
@@ -323,9 +234,15 @@ om_status om_merge_sort_u32(uint32_t* keys, uint32_t* vals, int64_t n, void* str
     if (vals != nullptr) {
         if ((reinterpret_cast<uintptr_t>(keys) & 15) != (reinterpret_cast<uintptr_t>(vals) & 15)) return OM_EINVAL;
         if (overlaps(keys, n, vals, n)) return OM_EINVAL;
-        return sort_impl<true>(keys, vals, n, (cudaStream_t)stream);
+        DeviceState* d = nullptr;
+        const om_status s = device_state(&d);
+        if (s != OM_OK) return s;
+        return sort_impl<uint32_t, true>(keys, vals, n, d->resident_merge_v, (cudaStream_t)stream);
     }
-    return sort_impl<false>(keys, nullptr, n, (cudaStream_t)stream);
+    DeviceState* d = nullptr;
+    const om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    return sort_impl<uint32_t, false>(keys, nullptr, n, d->resident_merge, (cudaStream_t)stream);
 }
 
 const char* om_status_string(int status) {

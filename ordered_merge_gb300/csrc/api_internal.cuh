@@ -10,6 +10,7 @@
 
 #include "merge_kernels.cuh"
 #include "ordmerge.h"
+#include "sort_kernels.cuh"
 
 namespace om {
 
@@ -53,6 +54,13 @@ struct CfgFor<double, false> {
 
 template <typename K, bool V>
 using SmemFor = TileSmem<typename CfgFor<K, V>::type, V, KeyGeom<K>::E>;
+
+//  sort: one block pass sorts 256 x 16 = 4096-element tiles in shared memory
+//        (runs of 16 in registers, then merges of whole pairs of runs per
+//        CTA through 1024 to 4096); later passes use
+//        the partition + tile-merge kernels on each pair of runs.
+using SmallMergeCfg = BlockSortCfg<256, 16>;
+constexpr int kEarlyTo = SmallMergeCfg::TILE;  // runs after the block pass: 4096
 
 enum KernelKind { kKindPartition = 0, kKindTileMerge = 1, kKindBlockSort = 2, kKindCorank = 3, kNumKinds = 4 };
 
@@ -157,6 +165,93 @@ om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, co
     cudaError_t ef = cudaFreeAsync(split, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return ef == cudaSuccess ? OM_OK : OM_ECUDA;
+}
+
+// Stable merge sort of keys[0..n) in place (values optional), in the
+// order DESC.  Pass schedule: one block pass sorts each 4096-element tile in
+// shared memory (early stages: many small merges per block); then one
+// co-rank-split late pass per doubling of the run length, each a partition +
+// tile merge over all pairs of runs.  `resident_per_sm`: tile-merge CTAs of
+// this instantiation resident per SM.
+template <typename K, bool V, bool DESC = false>
+om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cudaStream_t st) {
+    static_assert(block_sort_smem_bytes<SmallMergeCfg, K, V>() <= 48 * 1024,
+                  "the block pass fits the default shared-memory limit");
+    DeviceState* d = nullptr;
+    om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+
+    int passes = 0;  // global passes after the block pass
+    for (int64_t r = kEarlyTo; r < n; r *= 2) ++passes;
+    using Cfg = typename CfgFor<K, V>::type;
+    const int64_t subtiles = (n + Cfg::T - 1) / Cfg::T;
+    const int64_t resident = (int64_t)d->sm_count * (resident_per_sm > 0 ? resident_per_sm : 1);
+    const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
+    // splitter slots for the largest late pass (every pair gets the same
+    // number of ranges, including a short last pair), plus one
+    int64_t max_ranges = 1;
+    for (int64_t r = kEarlyTo; r < n; r *= 2) {
+        const int64_t npairs = (n + 2 * r - 1) / (2 * r);
+        const int64_t rps = (2 * r + range_len - 1) / range_len;
+        if (npairs * rps + 1 > max_ranges) max_ranges = npairs * rps + 1;
+    }
+
+    K* tk = nullptr;
+    uint32_t* tv = nullptr;
+    int64_t* split = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (passes > 0) {
+        e = cudaMallocAsync(reinterpret_cast<void**>(&tk), (size_t)n * sizeof(K), st);
+        if (e == cudaSuccess && V) e = cudaMallocAsync(reinterpret_cast<void**>(&tv), (size_t)n * 4, st);
+        if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&split), (size_t)max_ranges * 8, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            if (tk) cudaFreeAsync(tk, st);
+            if (tv) cudaFreeAsync(tv, st);
+            return OM_ENOMEM;
+        }
+    }
+    // The block pass writes where the pass count's parity makes the last
+    // pass land back in keys / vals.
+    K* src_k = (passes % 2 == 0) ? keys : tk;
+    uint32_t* src_v = (passes % 2 == 0) ? vals : tv;
+    K* dst_k = (passes % 2 == 0) ? tk : keys;
+    uint32_t* dst_v = (passes % 2 == 0) ? tv : vals;
+
+    {
+        // run sort and early merges in one launch: every CTA sorts 16
+        // elements per thread in registers, then merges runs 16 -> ... ->
+        // 1024 -> ... -> kEarlyTo in shared memory (whole pairs per CTA)
+        const unsigned grid = (unsigned)((n + SmallMergeCfg::TILE - 1) / SmallMergeCfg::TILE);
+        e = traced(kKindBlockSort, st, [&] {
+            block_sort_kernel<SmallMergeCfg, K, V, DESC>
+                <<<grid, SmallMergeCfg::NT, block_sort_smem_bytes<SmallMergeCfg, K, V>(), st>>>(
+                    keys, vals, src_k, src_v, n, 1, kEarlyTo);
+        });
+    }
+    for (int64_t r = kEarlyTo; e == cudaSuccess && r < n; r *= 2) {
+        // late pass: co-rank split of each pair of runs into output ranges
+        const int64_t npairs = (n + 2 * r - 1) / (2 * r);
+        const int64_t rps = (2 * r + range_len - 1) / range_len;
+        MergeGeom<K> g{src_k, src_v, nullptr, nullptr, dst_k, dst_v, n, 0, r, range_len, rps, npairs * rps};
+        if (g.nranges + 1 > max_ranges || g.nranges > 0x7fffffff) {
+            e = cudaErrorInvalidValue;
+            break;
+        }
+        e = launch_merge<K, V, DESC>(g, split, d, st);
+        K* t = src_k;
+        src_k = dst_k;
+        dst_k = t;
+        uint32_t* tq = src_v;
+        src_v = dst_v;
+        dst_v = tq;
+    }
+    if (passes > 0) {
+        cudaFreeAsync(split, st);
+        cudaFreeAsync(tk, st);
+        if (V) cudaFreeAsync(tv, st);
+    }
+    return e == cudaSuccess ? OM_OK : cuda_fail(e);
 }
 
 }  // namespace om

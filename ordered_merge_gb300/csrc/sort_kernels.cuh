@@ -11,9 +11,9 @@
 // consecutive elements and, in shared memory, takes every run of length
 // run_from inside the tile to length run_to by pairwise merges:
 //  * run_from == 1: each thread first sorts its VT consecutive elements in
-//    registers with an odd-even transposition network that only swaps on
-//    strictly greater keys (so equal keys keep their order), then merges
-//    upward from runs of VT.
+//    registers with an odd-even transposition network that only swaps when
+//    the left key comes strictly after the right one (so equal keys keep
+//    their order), then merges upward from runs of VT.
 //  * each merge step: thread t produces outputs [t*VT, t*VT + VT) of the
 //    merge its slice falls in (VT and the run lengths are powers of two, so a
 //    slice never straddles two merges), by a co-rank search in shared memory
@@ -21,18 +21,38 @@
 //    first).
 // The kernel may run in place (out == in): a CTA reads its whole tile before
 // it writes any of it, and tiles do not overlap.
-// Shared memory indices are padded by one word per 32 so that the
-// register -> shared writes of VT consecutive elements per thread hit 32
-// distinct banks.
+// Shared memory indices are padded by one element per 128 bytes so that the
+// register -> shared writes of VT consecutive elements per thread hit
+// distinct banks (4-byte keys: one per 32 elements; 8-byte keys: one per 16).
+// Keys of any type of merge_kernels.cuh sort in either order (the order and
+// compare forms come from there); values are 32-bit.
 #pragma once
 
 #include <cstdint>
+#include <limits>
 
+#include "merge_kernels.cuh"
 #include "om_ptx.cuh"
 
 namespace om {
 
 __device__ __forceinline__ int pad32(int x) { return x + (x >> 5); }
+
+// Padded index of an E-byte element: one element of padding per 128 bytes.
+template <typename K>
+__device__ __forceinline__ int padk(int x) {
+    return x + x / (128 / (int)sizeof(K));
+}
+
+// A key that no key comes strictly after in the order: the type's maximum
+// (ascending) or lowest value (descending); infinities for floats.
+template <typename K, bool DESC>
+__device__ __forceinline__ K last_key() {
+    if (std::numeric_limits<K>::has_infinity) {
+        return DESC ? -std::numeric_limits<K>::infinity() : std::numeric_limits<K>::infinity();
+    }
+    return DESC ? std::numeric_limits<K>::lowest() : std::numeric_limits<K>::max();
+}
 
 template <int NT_, int VT_>
 struct BlockSortCfg {
@@ -44,66 +64,69 @@ struct BlockSortCfg {
     static_assert(TILE % 32 == 0, "tile is whole bank rows");
 };
 
-template <typename Cfg, bool V>
+template <typename Cfg, typename K, bool V>
 constexpr size_t block_sort_smem_bytes() {
-    return (size_t)Cfg::PADDED * 4 * (V ? 2 : 1);
+    return (size_t)(Cfg::TILE + Cfg::TILE / (128 / sizeof(K))) * sizeof(K) + (V ? (size_t)Cfg::PADDED * 4 : 0);
 }
 
 // co_rank(d) of A = s[pad(a0 + x)], x < m and B = s[pad(b0 + x)], x < n:
 // the largest i in [max(0,d-n), min(d,m)] with i at the lower bound or
-// A[i-1] <= B[d-i], by power-of-two steps from `top` (a power of two with
-// 2 * top > min(d,m) - max(0,d-n)), so every thread of a pass takes the same
-// number of steps.
-__device__ __forceinline__ int corank_padded(int d, const uint32_t* s, int a0, int m, int b0, int n, int top) {
+// A[i-1] <= B[d-i] (in the order), by power-of-two steps from `top` (a
+// power of two with 2 * top > min(d,m) - max(0,d-n)), so every thread of a
+// pass takes the same number of steps.
+template <typename K, bool DESC>
+__device__ __forceinline__ int corank_padded(int d, const K* s, int a0, int m, int b0, int n, int top) {
     int lo = d - n > 0 ? d - n : 0;
     const int hi = d < m ? d : m;
     for (int step = top; step > 0; step >>= 1) {
         const int cand = lo + step;
-        if (cand <= hi && s[pad32(a0 + cand - 1)] <= s[pad32(b0 + d - cand)]) lo = cand;
+        if (cand <= hi && a_first<DESC>(s[padk<K>(a0 + cand - 1)], s[padk<K>(b0 + d - cand)])) lo = cand;
     }
     return lo;
 }
 
-template <typename Cfg, bool V>
-__global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const uint32_t* in_k, const uint32_t* in_v,
-                                                             uint32_t* out_k, uint32_t* out_v, int64_t n,
-                                                             int run_from, int run_to) {
+template <typename Cfg, typename K, bool V, bool DESC = false>
+__global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const K* in_k, const uint32_t* in_v, K* out_k,
+                                                             uint32_t* out_v, int64_t n, int run_from, int run_to) {
     constexpr int NT = Cfg::NT;
     constexpr int VT = Cfg::VT;
     constexpr int TILE = Cfg::TILE;
-    extern __shared__ __align__(16) uint32_t bsm[];
-    uint32_t* sk = bsm;
-    uint32_t* sv = V ? bsm + Cfg::PADDED : nullptr;
+    constexpr int PADDED_K = TILE + TILE / (128 / (int)sizeof(K));
+    static_assert(!V || sizeof(K) == 4, "values ride with 4-byte keys");
+    extern __shared__ __align__(16) unsigned char bsm_raw[];
+    K* sk = reinterpret_cast<K*>(bsm_raw);
+    uint32_t* sv = V ? reinterpret_cast<uint32_t*>(sk + PADDED_K) : nullptr;
 
     const int tid = threadIdx.x;
     const int64_t base = (int64_t)blockIdx.x * TILE;
     const int count = (int)((n - base) < TILE ? (n - base) : TILE);
 
     for (int p = tid; p < count; p += NT) {
-        sk[pad32(p)] = in_k[base + p];
+        sk[padk<K>(p)] = in_k[base + p];
         if (V) sv[pad32(p)] = in_v[base + p];
     }
     __syncthreads();
 
     const int p0 = tid * VT;
-    uint32_t k[VT];
+    K k[VT];
     uint32_t v[VT];
     int w = run_from;
     if (run_from == 1) {
-        // Registers: elements past the tile end get the largest key and stay
-        // behind every real element (swaps need a strictly greater key).
+        // Registers: elements past the tile end get a key that nothing comes
+        // strictly after, so they stay behind every real element (a swap
+        // needs the left key strictly after the right one in the order).
 #pragma unroll
         for (int i = 0; i < VT; ++i) {
             const bool real = p0 + i < count;
-            k[i] = real ? sk[pad32(p0 + i)] : 0xFFFFFFFFu;
+            k[i] = real ? sk[padk<K>(p0 + i)] : last_key<K, DESC>();
             if (V) v[i] = real ? sv[pad32(p0 + i)] : 0u;
         }
 #pragma unroll
         for (int round = 0; round < VT; ++round) {
 #pragma unroll
             for (int i = round & 1; i + 1 < VT; i += 2) {
-                if (k[i] > k[i + 1]) {
-                    const uint32_t tk = k[i];
+                if (!a_first<DESC>(k[i], k[i + 1])) {
+                    const K tk = k[i];
                     k[i] = k[i + 1];
                     k[i + 1] = tk;
                     if (V) {
@@ -118,7 +141,7 @@ __global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const uint32_t* in_
 #pragma unroll
         for (int i = 0; i < VT; ++i) {
             if (p0 + i < count) {
-                sk[pad32(p0 + i)] = k[i];
+                sk[padk<K>(p0 + i)] = k[i];
                 if (V) sv[pad32(p0 + i)] = v[i];
             }
         }
@@ -136,20 +159,22 @@ __global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const uint32_t* in_
             const int nb = nb_raw <= 0 ? 0 : (nb_raw < w ? nb_raw : w);
             const int b0 = a0 + w;
             cnt = (m + nb - d) < VT ? (m + nb - d) : VT;
-            const int a = corank_padded(d, sk, a0, m, b0, nb, w);
+            const int a = corank_padded<K, DESC>(d, sk, a0, m, b0, nb, w);
             // Serial merge with selects: A and B are adjacent runs, so one
             // index (clamped into the tile) reaches either head.  Take A
-            // unless A is exhausted or B's head is strictly smaller.
+            // unless A is exhausted or B's head comes strictly before it.
             int ia = a0 + a, ib = b0 + (d - a);
             const int ea = a0 + m, eb = b0 + nb;
             int x = ia < TILE - 1 ? ia : TILE - 1;
             int y = ib < TILE - 1 ? ib : TILE - 1;
-            uint32_t ak = sk[pad32(x)], bk = sk[pad32(y)];
+            K ak = sk[padk<K>(x)], bk = sk[padk<K>(y)];
+            auto ao = OrderKey<K>::of(ak);
+            auto bo = OrderKey<K>::of(bk);
             uint32_t av = V ? sv[pad32(x)] : 0u, bv = V ? sv[pad32(y)] : 0u;
 #pragma unroll
             for (int i = 0; i < VT; ++i) {
                 if (i < cnt) {
-                    const bool p = (ib >= eb) || (ia < ea && ak <= bk);
+                    const bool p = (ib >= eb) || (ia < ea && ord_first<DESC>(ao, bo));
                     k[i] = p ? ak : bk;
                     if (V) v[i] = p ? av : bv;
                     ia += p ? 1 : 0;
@@ -157,9 +182,12 @@ __global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const uint32_t* in_
                     if (i + 1 < VT) {
                         int idx = p ? ia : ib;
                         idx = idx < TILE - 1 ? idx : TILE - 1;
-                        const uint32_t nk = sk[pad32(idx)];
+                        const K nk = sk[padk<K>(idx)];
+                        const auto no = OrderKey<K>::of(nk);
                         ak = p ? nk : ak;
                         bk = p ? bk : nk;
+                        ao = p ? no : ao;
+                        bo = p ? bo : no;
                         if (V) {
                             const uint32_t nv = sv[pad32(idx)];
                             av = p ? nv : av;
@@ -173,7 +201,7 @@ __global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const uint32_t* in_
 #pragma unroll
         for (int i = 0; i < VT; ++i) {
             if (i < cnt) {
-                sk[pad32(p0 + i)] = k[i];
+                sk[padk<K>(p0 + i)] = k[i];
                 if (V) sv[pad32(p0 + i)] = v[i];
             }
         }
@@ -181,7 +209,7 @@ __global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const uint32_t* in_
     }
 
     for (int p = tid; p < count; p += NT) {
-        out_k[base + p] = sk[pad32(p)];
+        out_k[base + p] = sk[padk<K>(p)];
         if (V) out_v[base + p] = sv[pad32(p)];
     }
 }

@@ -101,3 +101,20 @@ def test_merge_keys_host_argument_checks():
     # overlap counts 8 bytes per element: C = [0x2000, 0x2040) meets B at 0x2020
     assert L.om_merge_keys(i64, 0, 0x1000, 4, 0x2020, 4, 0x2000, None) == om.OM_EINVAL
     assert L.om_merge_keys(i64, 0, None, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+
+
+def test_merge_sort_keys_host_argument_checks():
+    import ordered_merge_gb300 as om
+
+    L = om.lib()
+    i64, f32 = om.KEY_TYPES["i64"][0], om.KEY_TYPES["f32"][0]
+    assert L.om_merge_sort_keys(9, 0, 0x1000, None, 16, None) == om.OM_EINVAL
+    assert L.om_merge_sort_keys(f32, 3, 0x1000, None, 16, None) == om.OM_EINVAL
+    assert L.om_merge_sort_keys(f32, 0, None, None, 1, None) == om.OM_OK       # trivial
+    assert L.om_merge_sort_keys(f32, 0, None, None, -1, None) == om.OM_EINVAL
+    assert L.om_merge_sort_keys(f32, 0, None, None, 16, None) == om.OM_EINVAL
+    assert L.om_merge_sort_keys(i64, 0, 0x1004, None, 16, None) == om.OM_EINVAL  # 8-byte alignment
+    assert L.om_merge_sort_keys(i64, 0, 0x1000, 0x9000, 16, None) == om.OM_EINVAL  # no values with 8-byte keys
+    assert L.om_merge_sort_keys(f32, 0, 0x1000, 0x2004, 16, None) == om.OM_EINVAL  # 16-byte phase differs
+    assert L.om_merge_sort_keys(f32, 1, 0x1000, 0x1010, 16, None) == om.OM_EINVAL  # overlap
+    assert L.om_merge_sort_keys(f32, 0, 0x1000, None, (1 << 40) + 1, None) == om.OM_ERANGE

@@ -1,6 +1,7 @@
-"""GPU parity of om_merge_keys (six key types, ascending and descending)
-against the CPU oracle: element by element, bit for bit, with guard bands
-around every output.
+"""GPU parity of om_merge_keys and om_merge_sort_keys (six key types,
+ascending and descending) against the CPU oracle: element by element, bit
+for bit, with guard bands around every merge output; values (index tags)
+make the sort's stability visible.
 
 Sizes span one sub-tile, many sub-tiles and output ranges, and ragged
 tails; edge cases cover empty and one-element sides, heavy ties, -0.0 and
@@ -191,3 +192,79 @@ def test_wide_keys_large(gpu, name):
     for desc in (False, True):
         check(gpu, name, sorted_keys(rng, name, (1 << 23) + 3, 1 << 30, desc),
               sorted_keys(rng, name, (1 << 23) - 3, 1 << 30, desc), desc)
+
+
+# ------------------------------------------------------------------- sort --
+
+def run_sort(om, name, keys, with_vals, desc):
+    dk = to_dev(keys, name)
+    dv = torch.from_numpy(np.arange(keys.size, dtype=np.int32)).cuda() if with_vals else None
+    om.merge_sort_keys(dk, dv, key_type=name, descending=desc)
+    torch.cuda.synchronize()
+    assert om.device_error() == 0
+    return dk.cpu().numpy().view(NP[name]), (dv.cpu().numpy().view(np.uint32) if with_vals else None)
+
+
+def check_sort(om, name, keys, desc, with_vals=None):
+    keys = np.ascontiguousarray(keys, dtype=NP[name])
+    if with_vals is None:
+        with_vals = np.dtype(NP[name]).itemsize == 4
+    gk, gv = run_sort(om, name, keys, with_vals, desc)
+    wk, wv = oracle.merge_sort_keys(keys, np.arange(keys.size, dtype=np.uint32), descending=desc)
+    npc, _ = _carrier(name)
+    if not np.array_equal(gk.view(npc), wk.view(npc)):
+        bad = int(np.flatnonzero(gk.view(npc) != wk.view(npc))[0])
+        raise AssertionError(f"{name} desc={desc} n={keys.size}: keys differ first at {bad}: "
+                             f"got {gk[bad]!r}, want {wk[bad]!r}")
+    if with_vals:
+        assert np.array_equal(gv, wv), f"values differ first at {int(np.flatnonzero(gv != wv)[0])}"
+
+
+def unsorted_keys(rng, name, size, span):
+    x = sorted_keys(rng, name, size, span, False)
+    return x[rng.permutation(size)]
+
+
+@pytest.mark.parametrize("desc", [False, True], ids=["asc", "desc"])
+@pytest.mark.parametrize("name", TYPES)
+@pytest.mark.parametrize("n", [0, 1, 2, 17, 4095, 4096, 4097, 10000, 100003, (1 << 18) + 12345])
+def test_sort_sizes(gpu, name, desc, n):
+    rng = np.random.default_rng(n + 13 * TYPES.index(name) + desc)
+    check_sort(gpu, name, unsorted_keys(rng, name, n, 1 << 30), desc)
+
+
+@pytest.mark.parametrize("desc", [False, True], ids=["asc", "desc"])
+@pytest.mark.parametrize("name", TYPES)
+def test_sort_heavy_ties_and_extremes(gpu, name, desc):
+    rng = np.random.default_rng(5 + TYPES.index(name) + 100 * desc)
+    check_sort(gpu, name, unsorted_keys(rng, name, 300007, 4), desc)
+    dt = NP[name]
+    if np.issubdtype(dt, np.floating):
+        vals = np.array([-np.inf, -1.0, -0.0, 0.0, np.finfo(dt).smallest_subnormal, np.inf], dt)
+    else:
+        info = np.iinfo(dt)
+        vals = np.array([info.min, info.min + 1, 0, 1, info.max - 1, info.max], dt)
+    check_sort(gpu, name, vals[rng.integers(0, vals.size, 200003)], desc)
+
+
+@pytest.mark.parametrize("name", TYPES)
+def test_sort_presorted_reversed_keys_only(gpu, name):
+    rng = np.random.default_rng(TYPES.index(name))
+    x = sorted_keys(rng, name, 150001, 1 << 30, False)
+    for desc in (False, True):
+        check_sort(gpu, name, x, desc)
+        check_sort(gpu, name, x[::-1].copy(), desc)
+        check_sort(gpu, name, unsorted_keys(rng, name, 70001, 100), desc, with_vals=False)
+
+
+def test_sort_u32_typed_matches_merge_sort_u32(gpu):
+    """The typed call on uint32 keys ascending gives om_merge_sort_u32's output."""
+    rng = np.random.default_rng(2)
+    keys = rng.integers(0, 1 << 32, 300001, dtype=np.uint64).astype(np.uint32)
+    vals = np.arange(keys.size, dtype=np.uint32)
+    k1, v1 = to_dev(keys, "u32"), torch.from_numpy(vals.view(np.int32)).cuda()
+    k2, v2 = k1.clone(), v1.clone()
+    gpu.merge_sort_u32(k1, v1)
+    gpu.merge_sort_keys(k2, v2, key_type="u32")
+    torch.cuda.synchronize()
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
