@@ -47,15 +47,23 @@ WORKLOADS = {
     "skewed": "int32 merge, A = 2^28 sorted full-range, B = 2^10 sorted in [-2^20, 2^20]",
     "pairs_ties": "uint32 key+value merge, m = n = 2^24, keys in [0,16)",
     "sort": "stable merge sort of 2^26 uint32 keys with index payload",
+    "f64": "float64 merge: A, B = 2^27 sorted float64 each (int32 draws x 2^-20)",
+    "i64_desc": "int64 merge, descending: A, B = 2^27 full-range int64 each, sorted nonincreasing",
+    "sort_f32_desc": "stable descending merge sort of 2^26 float32 keys with index payload",
+    "sort_f64": "stable merge sort of 2^26 float64 keys, keys only",
 }
+SORTS = ("sort", "sort_f32_desc", "sort_f64")
 
 # Source files whose change invalidates a recorded ncu traffic figure.
 KERNEL_SOURCES = [
     "ordered_merge_gb300/csrc/merge_kernels.cuh",
+    "ordered_merge_gb300/csrc/sort_kernels.cuh",
     "ordered_merge_gb300/csrc/om_ptx.cuh",
+    "ordered_merge_gb300/csrc/api_internal.cuh",
     "ordered_merge_gb300/csrc/api.cu",
+    "ordered_merge_gb300/csrc/typed_merge.cu",
 ]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tile_merge_uniform_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tile_merge_traffic.json")
 
 
 def kernel_source_hash() -> str:
@@ -67,16 +75,18 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """Per-launch DRAM bytes of the tile-merge kernel from a committed ncu
-    summary, or None when there is none or the kernel changed since."""
+    """Per-launch DRAM bytes (read + write) of the tile-merge kernel on this
+    workload from the committed ncu summary, or None when there is none or
+    the kernel sources changed since it was taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("workload") != workload or rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash():
         return None
-    return rec.get("traffic_bytes_per_launch")
+    wl = rec.get("workloads", {}).get(workload)
+    return wl.get("traffic_bytes_per_launch") if wl else None
 
 
 def load_peak():
@@ -205,21 +215,40 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle --
 
-def oracle_rate(A, B, budget_s: float = 12.0, max_reps: int = 5):
-    """Elements/s of the single-thread oracle merge on host arrays A, B."""
+def oracle_call(wl: str, h: dict):
+    """(callable, units): one run of the CPU oracle on host arrays `h` of
+    workload `wl` (a merge, or a sort from the unsorted keys), and the
+    elements it produces."""
     import oracle
+    import synth
 
     lib = oracle.load()
+    if wl in ("uniform", "evens_odds", "skewed"):
+        return (lambda: oracle.merge_i32(h["A"], h["B"], lib=lib)), h["A"].size + h["B"].size
+    if wl == "pairs_ties":
+        return ((lambda: oracle.merge_pairs_u32(h["keysA"], h["valsA"], h["keysB"], h["valsB"], lib=lib)),
+                h["keysA"].size + h["keysB"].size)
+    if wl == "sort":
+        return (lambda: oracle.merge_sort_pairs_u32(h["keys"], h["vals"], lib=lib)), h["keys"].size
+    kt, desc = synth.TYPED[wl]
+    if "A" in h:
+        return (lambda: oracle.merge_keys(h["A"], h["B"], descending=desc, lib=lib)), h["A"].size + h["B"].size
+    return (lambda: oracle.merge_sort_keys(h["keys"], h.get("vals"), descending=desc, lib=lib)), h["keys"].size
+
+
+def oracle_rate(wl: str, h: dict, budget_s: float = 12.0, max_reps: int = 5):
+    """Elements/s of the single-thread oracle on host arrays of workload wl."""
+    fn, units = oracle_call(wl, h)
     times = []
     t_start = time.perf_counter()
     while len(times) < max_reps:
         t0 = time.perf_counter()
-        oracle.merge_i32(A, B, lib=lib)
+        fn()
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_start > budget_s:
             break
     best = statistics.median(times)
-    return (A.size + B.size) / best, len(times), best
+    return units / best, len(times), best, units
 
 
 # ------------------------------------------------------------- our arm --
@@ -248,6 +277,15 @@ def bench_ours(args):
         C = torch.empty(total, dtype=torch.int32, device=device)
         step = lambda: om.merge_i32(A, B, C)
         units_per_step = total
+    elif wl in ("f64", "i64_desc"):
+        kt, desc = synth.TYPED[wl]
+        A, B = d["A"], d["B"]
+        m, n = A.numel(), B.numel()
+        total = m + n
+        bytes_per_elem = 2 * A.element_size()
+        C = torch.empty(total, dtype=A.dtype, device=device)
+        step = lambda: om.merge_keys(A, B, C, key_type=kt, descending=desc)
+        units_per_step = total
     elif wl == "pairs_ties":
         ka, va, kb, vb = d["keysA"], d["valsA"], d["keysB"], d["valsB"]
         m, n = ka.numel(), kb.numel()
@@ -257,14 +295,28 @@ def bench_ours(args):
         vc = torch.empty_like(kc)
         step = lambda: om.merge_pairs_u32(ka, va, kb, vb, kc, vc)
         units_per_step = total
-    else:  # sort: restore the unsorted input before each step (outside the timed events)
-        keys0, vals0 = d["keys"], d["vals"]
+    else:  # sorts: restore the unsorted input before each step (outside the timed events)
+        keys0, vals0 = d["keys"], d.get("vals")
         m, n = keys0.numel(), 0
         total = m
-        bytes_per_elem = 16
-        keys, vals = keys0.clone(), vals0.clone()
+        # per element of one late pass: key read + written, value read + written
+        bytes_per_elem = 2 * keys0.element_size() + (8 if vals0 is not None else 0)
+        keys = keys0.clone()
+        vals = vals0.clone() if vals0 is not None else None
+        kt, desc = synth.TYPED.get(wl, ("u32", False))
         step = None
         units_per_step = total
+
+        def sort_once():
+            keys.copy_(keys0)
+            if vals is not None:
+                vals.copy_(vals0)
+
+        def sort_call():
+            if wl == "sort":
+                om.merge_sort_u32(keys, vals)
+            else:
+                om.merge_sort_keys(keys, vals, key_type=kt, descending=desc)
 
     # ---- warm-up, then K timed steps
     if step is not None:
@@ -291,9 +343,8 @@ def bench_ours(args):
         ms = ev0.elapsed_time(ev1)
     else:
         for _ in range(args.warmup):
-            keys.copy_(keys0)
-            vals.copy_(vals0)
-            om.merge_sort_u32(keys, vals)
+            sort_once()
+            sort_call()
         torch.cuda.synchronize(device)
         barrier(world, device)
         om.om_trace_reset()
@@ -302,12 +353,11 @@ def bench_ours(args):
         ms = 0.0
         with ClockSampler(local) as clk:
             for _ in range(args.steps):
-                keys.copy_(keys0)
-                vals.copy_(vals0)
+                sort_once()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                om.merge_sort_u32(keys, vals)
+                sort_call()
                 e1.record(stream)
                 e1.synchronize()
                 ms += e0.elapsed_time(e1)
@@ -325,12 +375,10 @@ def bench_ours(args):
     p_launches, p_ms = om.om_trace_read(om.KIND_PARTITION)
     bs_launches, bs_ms = om.om_trace_read(om.KIND_BLOCK_SORT)
     peak, peak_src = load_peak()
-    if wl == "sort":
-        # dominant kernel: the late-pass tile merge; per launch it moves one
-        # pass of n elements: 8 B read + 8 B written
-        alg_bytes = total * 16
-    else:
-        alg_bytes = total * bytes_per_elem
+    # merges: one launch moves every element once (read + written); sorts: the
+    # dominant kernel is the late-pass tile merge, one pass of n elements per
+    # launch.  Either way total * bytes_per_elem per launch.
+    alg_bytes = total * bytes_per_elem
     tm_avg_ms = tm_ms / tm_launches if tm_launches else float("nan")
     achieved = alg_bytes / (tm_avg_ms / 1e3) / 1e9 if tm_launches else None
     traffic = recorded_traffic(wl)
@@ -424,18 +472,17 @@ def bench_ours(args):
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl in ("uniform", "evens_odds", "skewed"):
-        import oracle  # noqa: F401  (test infrastructure: the baseline leg only)
-
-        hA_np = A.cpu().numpy()
-        hB_np = B.cpu().numpy()
-        rate, reps, best = oracle_rate(hA_np, hB_np)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle (test infrastructure: the baseline leg only) on the same
+        # seeded workload, built on the host
+        h = synth.make_host(wl, scale_log2=args.scale_log2)
+        rate, reps, best, units = oracle_rate(wl, h)
         cpu = {
             "value": rate,
             "unit": UNIT,
             "cores": 1,
             "kind": "oracle",
-            "sample": f"the full workload ({total} outputs), median of {reps} single-thread oracle merges "
+            "sample": f"the full workload ({units} outputs), median of {reps} single-thread oracle runs "
                       f"({best:.2f} s each)",
             "host_threads_available": os.cpu_count(),
         }
@@ -452,7 +499,8 @@ def bench_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "int32" if wl in ("uniform", "evens_odds", "skewed") else "u32",
+            "dtype": {"f64": "f64", "i64_desc": "int64", "sort_f32_desc": "f32", "sort_f64": "f64"}.get(
+                wl, "int32" if wl in ("uniform", "evens_odds", "skewed") else "u32"),
             "data": "synthetic (seeded SplitMix64, sorted on device)",
             "config": {
                 "workload": WORKLOADS[wl],
@@ -464,8 +512,8 @@ def bench_ours(args):
                       "inputs smaller than L2: back-to-back steps may hit L2",
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
-            "achieved_gbs": round(units_per_step * (bytes_per_elem if wl != "sort" else 16) * args.steps
-                                  / (ms / 1e3) / 1e9, 1) if wl != "sort" else None,
+            "achieved_gbs": round(units_per_step * bytes_per_elem * args.steps
+                                  / (ms / 1e3) / 1e9, 1) if wl not in SORTS else None,
             "roofline": roofline,
             "kernel_time_ms": kernel_share,
             "e2e": e2e,
@@ -487,32 +535,28 @@ def bench_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import numpy as np
-
-    import oracle
     import synth
 
-    lib = oracle.load()
+    wl = args.workload
     # per-step sample: same recipe, scaled so all K + W steps take about
-    # --ref-budget-s seconds on one core
+    # --ref-budget-s seconds on one core (a sort costs about log2(n) merges)
     budget_s = float(args.ref_budget_s)
-    rate_guess = 2.5e8
+    full = sum(synth.sizes(wl, 0))
+    rate_guess = 2.5e8 / (max(1, full.bit_length() - 12) if wl in SORTS else 1)
     per_step = budget_s * rate_guess / max(1, args.steps + args.warmup)
     scale = 0
-    total_full = sum(synth.sizes(args.workload if args.workload != "sort" else "uniform", 0))
-    while total_full >> scale > per_step and scale < 20:
+    while full >> scale > per_step and scale < 20:
         scale += 1
-    wl = args.workload if args.workload in ("uniform", "evens_odds", "skewed") else "uniform"
     d = synth.make_host(wl, scale_log2=scale)
-    A, B = d["A"], d["B"]
+    fn, total = oracle_call(wl, d)
     for _ in range(args.warmup):
-        oracle.merge_i32(A, B, lib=lib)
+        fn()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.merge_i32(A, B, lib=lib)
+        fn()
     dt = time.perf_counter() - t0
-    total = A.size + B.size
     value = total * args.steps / dt
+    m, n = synth.sizes(wl, scale)
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -525,9 +569,10 @@ def bench_reference(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int32",
+        "dtype": {"f64": "f64", "i64_desc": "int64", "sort_f32_desc": "f32", "sort_f64": "f64"}.get(
+            wl, "int32" if wl in ("uniform", "evens_odds", "skewed") else "u32"),
         "data": "synthetic (seeded SplitMix64)",
-        "config": {"workload": WORKLOADS[wl], "name": wl, "m": int(A.size), "n": int(B.size),
+        "config": {"workload": WORKLOADS[wl], "name": wl, "m": int(m), "n": int(n),
                    "sample_scale_log2": scale, "parallelism": "host CPU, 1 thread"},
         "cpu_baseline": {
             "value": value,

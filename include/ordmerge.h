@@ -32,8 +32,11 @@
  *    kernels run surface at the caller's next synchronisation, and in
  *    om_device_error().
  *  - Scratch (co-rank splitter arrays; the sort's second buffer) is taken
- *    with cudaMallocAsync on `stream` and released with cudaFreeAsync on the
- *    same stream, so it is stream-ordered; failure returns OM_ENOMEM.
+ *    from the library's own stream-ordered memory pool on `stream`
+ *    (cudaMallocFromPoolAsync) and freed on the same stream (cudaFreeAsync),
+ *    so it is stream-ordered; failure returns OM_ENOMEM.  The pool keeps
+ *    freed scratch mapped for later calls, so a device holds up to the
+ *    largest scratch any call needed until om_release_scratch().
  *  - No call exits the process or prints.  A failing call returns a status.
  */
 #ifndef ORDMERGE_H
@@ -130,6 +133,12 @@ om_status om_device_error(void *stream, uint32_t *detail);
 om_status om_trace_enable(int on);
 om_status om_trace_reset(void);
 om_status om_trace_read(int kind, int64_t *launches, double *total_ms);
+
+/*
+ * Returns the scratch the library's pool holds on the current device to the
+ * system (waits for the device first).  Later calls map it again as needed.
+ */
+om_status om_release_scratch(void);
 
 /* Number of kernels this library has launched since load. */
 uint64_t om_launch_count(void);

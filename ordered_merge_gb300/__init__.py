@@ -66,6 +66,8 @@ def _load():
     lib.om_merge_keys.restype = I32
     lib.om_merge_sort_keys.argtypes = [I32, I32, P, P, I64, P]
     lib.om_merge_sort_keys.restype = I32
+    lib.om_release_scratch.argtypes = []
+    lib.om_release_scratch.restype = I32
     lib.om_launch_count.argtypes = []
     lib.om_launch_count.restype = ctypes.c_uint64
     return lib
@@ -280,6 +282,11 @@ def om_trace_read(kind: int):
     return int(n.value), float(ms.value)
 
 
+def om_release_scratch():
+    """Return the library's cached scratch on the current device to the system."""
+    _check(_lib.om_release_scratch(), "om_release_scratch")
+
+
 def om_launch_count() -> int:
     return int(_lib.om_launch_count())
 
@@ -292,3 +299,4 @@ merge_keys = om_merge_keys
 merge_sort_keys = om_merge_sort_keys
 merge_sort_u32 = om_merge_sort_u32
 device_error = om_device_error
+release_scratch = om_release_scratch

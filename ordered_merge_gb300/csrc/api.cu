@@ -53,6 +53,24 @@ om_status device_state(DeviceState** out) {
         if (e != cudaSuccess) return OM_ECUDA;
         if (d.resident_merge < 1) d.resident_merge = 1;
         if (d.resident_merge_v < 1) d.resident_merge_v = 1;
+        // Scratch pool: freed scratch stays mapped for the next call, so a
+        // sort does not map and unmap its second buffer every time the
+        // caller synchronises (which a pool with the default threshold of 0
+        // would do).
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return OM_ECUDA;
+        }
+        uint64_t keep = UINT64_MAX;
+        if (cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaGetLastError();
+            return OM_ECUDA;
+        }
         d.ready = true;
     }
     *out = &d;
@@ -296,6 +314,14 @@ om_status om_trace_read(int kind, int64_t* launches, double* total_ms) {
 }
 
 uint64_t om_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+om_status om_release_scratch(void) {
+    DeviceState* d = nullptr;
+    const om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    if (cudaDeviceSynchronize() != cudaSuccess) return OM_ECUDA;
+    return cudaMemPoolTrimTo(d->pool, 0) == cudaSuccess ? OM_OK : OM_ECUDA;
+}
 
 // ------------------------------------------------- merge without allocating --
 //

@@ -73,11 +73,21 @@ struct DeviceState {
     int resident_merge_v = 0;
     uint32_t* err = nullptr;
     int64_t* corank_slot = nullptr;
+    cudaMemPool_t pool = nullptr;  // the library's scratch pool on this device
 };
 
 // Per-device set-up, once per device (thread-safe): SM count, addresses of
-// the library's device words, shared-memory limits of the kernels.
+// the library's device words, shared-memory limits of the kernels, the
+// scratch pool.
 om_status device_state(DeviceState** out);
+
+// Stream-ordered scratch from the library's own memory pool.  The pool keeps
+// freed memory mapped for the next call (release threshold: unlimited) until
+// om_release_scratch() trims it; the caller's default pool is not touched.
+inline cudaError_t scratch_alloc(const DeviceState* d, void** p, size_t bytes, cudaStream_t st) {
+    return cudaMallocFromPoolAsync(p, bytes, d->pool, st);
+}
+inline cudaError_t scratch_free(void* p, cudaStream_t st) { return cudaFreeAsync(p, st); }
 
 // ----------------------------------------------------------------- tracing --
 
@@ -156,13 +166,13 @@ om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, co
     if (nranges > 0x7fffffff) return OM_ERANGE;
     MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
     int64_t* split = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&split), (size_t)(nranges + 1) * 8, st);
+    cudaError_t e = scratch_alloc(d, reinterpret_cast<void**>(&split), (size_t)(nranges + 1) * 8, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return OM_ENOMEM;
     }
     e = launch_merge<K, V, DESC>(g, split, d, st);
-    cudaError_t ef = cudaFreeAsync(split, st);
+    cudaError_t ef = scratch_free(split, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return ef == cudaSuccess ? OM_OK : OM_ECUDA;
 }
@@ -201,13 +211,13 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
     int64_t* split = nullptr;
     cudaError_t e = cudaSuccess;
     if (passes > 0) {
-        e = cudaMallocAsync(reinterpret_cast<void**>(&tk), (size_t)n * sizeof(K), st);
-        if (e == cudaSuccess && V) e = cudaMallocAsync(reinterpret_cast<void**>(&tv), (size_t)n * 4, st);
-        if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&split), (size_t)max_ranges * 8, st);
+        e = scratch_alloc(d, reinterpret_cast<void**>(&tk), (size_t)n * sizeof(K), st);
+        if (e == cudaSuccess && V) e = scratch_alloc(d, reinterpret_cast<void**>(&tv), (size_t)n * 4, st);
+        if (e == cudaSuccess) e = scratch_alloc(d, reinterpret_cast<void**>(&split), (size_t)max_ranges * 8, st);
         if (e != cudaSuccess) {
             cudaGetLastError();
-            if (tk) cudaFreeAsync(tk, st);
-            if (tv) cudaFreeAsync(tv, st);
+            if (tk) scratch_free(tk, st);
+            if (tv) scratch_free(tv, st);
             return OM_ENOMEM;
         }
     }
@@ -247,9 +257,9 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
         dst_v = tq;
     }
     if (passes > 0) {
-        cudaFreeAsync(split, st);
-        cudaFreeAsync(tk, st);
-        if (V) cudaFreeAsync(tv, st);
+        scratch_free(split, st);
+        scratch_free(tk, st);
+        if (V) scratch_free(tv, st);
     }
     return e == cudaSuccess ? OM_OK : cuda_fail(e);
 }

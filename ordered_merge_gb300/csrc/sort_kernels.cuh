@@ -38,10 +38,12 @@ namespace om {
 
 __device__ __forceinline__ int pad32(int x) { return x + (x >> 5); }
 
-// Padded index of an E-byte element: one element of padding per 128 bytes.
+// Padded index of an E-byte element (x >= 0): one element of padding per
+// 128 bytes, i.e. per 32 four-byte or 16 eight-byte elements.
 template <typename K>
 __device__ __forceinline__ int padk(int x) {
-    return x + x / (128 / (int)sizeof(K));
+    static_assert(sizeof(K) == 4 || sizeof(K) == 8, "keys of 4 or 8 bytes");
+    return x + (x >> (sizeof(K) == 4 ? 5 : 4));
 }
 
 // A key that no key comes strictly after in the order: the type's maximum

@@ -28,6 +28,16 @@ Workloads (lengths in elements):
 4. ``uniform``: A, B = 2^28 sorted full-range int32 each.
 5. ``sort``: 2^26 full-range uint32 keys (unsorted), values = 0 .. n-1.
 
+Other key types and descending order (same bytes per merge as ``uniform``):
+
+6. ``f64``: A, B = 2^27 sorted float64 each, value = a full-range int32 draw
+   times 2^-20 (exact; negatives, both signs).
+7. ``i64_desc``: A, B = 2^27 int64 each, sorted nonincreasing, value =
+   (top 32 bits of one draw) << 32 | (top 32 bits of a second stream's draw).
+8. ``sort_f32_desc``: 2^26 float32 keys (a full-range int32 draw times 2^-8,
+   rounded to float32), values = 0 .. n-1, to be sorted nonincreasing.
+9. ``sort_f64``: 2^26 float64 keys (int32 draw times 2^-20), keys only.
+
 Every length can be scaled down for tests (``scale_log2``), keeping the
 value distribution and structure.
 """
@@ -43,9 +53,11 @@ GOLDEN_GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-SEEDS = {"evens_odds": 1, "pairs_ties": 2, "skewed": 3, "uniform": 4, "sort": 5}
+SEEDS = {"evens_odds": 1, "pairs_ties": 2, "skewed": 3, "uniform": 4, "sort": 5,
+         "f64": 6, "i64_desc": 7, "sort_f32_desc": 8, "sort_f64": 9}
 
-WORKLOADS = ("evens_odds", "pairs_ties", "skewed", "uniform", "sort")
+WORKLOADS = ("evens_odds", "pairs_ties", "skewed", "uniform", "sort", "f64", "i64_desc", "sort_f32_desc",
+             "sort_f64")
 
 
 def side_seed(workload: str, side: int) -> int:
@@ -153,8 +165,10 @@ def sizes(workload: str, scale_log2: int = 0) -> tuple[int, int]:
         return 1 << (28 - s), 1 << max(0, 10 - s)
     if workload == "uniform":
         return 1 << (28 - s), 1 << (28 - s)
-    if workload == "sort":
+    if workload in ("sort", "sort_f32_desc", "sort_f64"):
         return 1 << (26 - s), 0
+    if workload in ("f64", "i64_desc"):
+        return 1 << (27 - s), 1 << (27 - s)
     raise ValueError(workload)
 
 
@@ -185,6 +199,41 @@ def host_sorted(x: np.ndarray) -> np.ndarray:
     return np.sort(x, kind="stable")
 
 
+def raw_f64_scaled(seed: int, count: int, shift: int = 20) -> np.ndarray:
+    """Full-range int32 draws times 2^-shift, as float64 (exact)."""
+    return np.ldexp(uniform_i32(seed, count).astype(np.float64), -shift)
+
+
+def raw_f32_scaled(seed: int, count: int, shift: int = 8) -> np.ndarray:
+    """Full-range int32 draws times 2^-shift, rounded to float32."""
+    return np.ldexp(uniform_i32(seed, count).astype(np.float64), -shift).astype(np.float32)
+
+
+def raw_i64_full(seed: int, count: int) -> np.ndarray:
+    """Full-range int64: top 32 bits of one stream, low 32 of a second."""
+    hi = uniform_u32(seed, count).astype(np.uint64) << np.uint64(32)
+    lo = uniform_u32(seed ^ (1 << 12), count).astype(np.uint64)
+    return (hi | lo).view(np.int64)
+
+
+def _typed_raw(workload: str, sa: int, sb: int, m: int, n: int):
+    """Unsorted raw arrays of the typed workloads (None for B of a sort)."""
+    if workload == "f64":
+        return raw_f64_scaled(sa, m), raw_f64_scaled(sb, n)
+    if workload == "i64_desc":
+        return raw_i64_full(sa, m), raw_i64_full(sb, n)
+    if workload == "sort_f32_desc":
+        return raw_f32_scaled(sa, m), None
+    if workload == "sort_f64":
+        return raw_f64_scaled(sa, m), None
+    raise ValueError(workload)
+
+
+# key type and order of the typed workloads
+TYPED = {"f64": ("f64", False), "i64_desc": ("i64", True), "sort_f32_desc": ("f32", True),
+         "sort_f64": ("f64", False)}
+
+
 # ------------------------------------------------------------- workloads --
 
 def make_host(workload: str, scale_log2: int = 0, seed_offset: int = 0) -> dict:
@@ -212,6 +261,18 @@ def make_host(workload: str, scale_log2: int = 0, seed_offset: int = 0) -> dict:
         return {"keysA": ka, "valsA": va, "keysB": kb, "valsB": vb}
     if workload == "sort":
         return {"keys": uniform_u32(sa, m), "vals": np.arange(m, dtype=np.uint32)}
+    if workload in TYPED:
+        ra, rb = _typed_raw(workload, sa, sb, m, n)
+        desc = TYPED[workload][1]
+        if rb is None:
+            out = {"keys": ra}
+            if workload == "sort_f32_desc":
+                out["vals"] = np.arange(m, dtype=np.uint32)
+            return out
+        A, B = host_sorted(ra), host_sorted(rb)
+        if desc:
+            A, B = A[::-1].copy(), B[::-1].copy()
+        return {"A": A, "B": B}
     raise ValueError(workload)
 
 
@@ -255,4 +316,18 @@ def make_device(workload: str, device, scale_log2: int = 0, seed_offset: int = 0
         return {"keysA": ka, "valsA": va, "keysB": kb, "valsB": vb}
     if workload == "sort":
         return {"keys": dev(uniform_u32(sa, m)), "vals": torch.arange(m, dtype=torch.int32, device=device)}
+    if workload in TYPED:
+        # typed tensors (float64 / int64 / float32); sorted with torch.sort,
+        # whose values equal numpy's for these (no NaN; the only equal keys
+        # with different bits, -0.0 and +0.0, cannot occur: zero draws give +0.0)
+        ra, rb = _typed_raw(workload, sa, sb, m, n)
+        desc = TYPED[workload][1]
+        if rb is None:
+            out = {"keys": torch.from_numpy(ra).to(device)}
+            if workload == "sort_f32_desc":
+                out["vals"] = torch.arange(m, dtype=torch.int32, device=device)
+            return out
+        A = torch.sort(torch.from_numpy(ra).to(device), descending=desc).values
+        B = torch.sort(torch.from_numpy(rb).to(device), descending=desc).values
+        return {"A": A, "B": B}
     raise ValueError(workload)

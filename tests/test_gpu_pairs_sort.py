@@ -139,3 +139,20 @@ def test_pairs_long_ranges_uneven_consumption(gpu, monkeypatch, per_range):
     ka, kb = keys[labels == 0], keys[labels == 1]
     va, vb = tagged(ka.size, kb.size)
     check_pairs(gpu, ka, va, kb, vb)
+
+
+def test_scratch_pool_reuse_and_release(gpu):
+    """Sorts reuse the library's scratch pool across synchronising calls;
+    om_release_scratch hands the cached scratch back (device free memory
+    grows by at least the sort's second buffer) and later sorts still work."""
+    rng = np.random.default_rng(77)
+    n = 1 << 22
+    keys = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    check_sort(gpu, keys)
+    check_sort(gpu, keys)
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    gpu.release_scratch()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after - free_before >= 2 * n * 4 - (2 << 20)
+    check_sort(gpu, keys)

@@ -34,3 +34,23 @@ def test_workload_shapes():
     assert d["keys"].size == 1 << 12 and np.array_equal(d["vals"], np.arange(1 << 12, dtype=np.uint32))
     u = synth.make_host("uniform", 16)
     assert u["A"].size == 1 << 12 and not np.array_equal(u["A"], u["B"])
+
+
+def test_typed_workloads_host_equals_device_on_cpu():
+    """The typed workloads: host arrays sorted in their order, and the device
+    path (here torch on the CPU) gives the same bits."""
+    import torch
+
+    for wl, (kt, desc) in synth.TYPED.items():
+        h = synth.make_host(wl, 12)
+        d = synth.make_device(wl, torch.device("cpu"), 12)
+        for key in h:
+            hv = h[key]
+            dv = d[key].numpy()
+            assert hv.dtype.itemsize == dv.dtype.itemsize
+            assert np.array_equal(hv.view(np.uint8), np.ascontiguousarray(dv).view(np.uint8)), (wl, key)
+        if "A" in h:
+            for arr in (h["A"], h["B"]):
+                diffs = np.diff(arr.astype(np.float64)) if arr.dtype.kind == "f" else np.diff(arr.astype(object))
+                assert all(x <= 0 for x in diffs) if desc else all(x >= 0 for x in diffs)
+        assert synth.sizes(wl, 12)[0] == h["A" if "A" in h else "keys"].size
