@@ -31,8 +31,9 @@
  *    host: they validate, enqueue and return.  Errors raised while the
  *    kernels run surface at the caller's next synchronisation, and in
  *    om_device_error().
- *  - Scratch (co-rank splitter arrays; the sort's second buffer) is taken
- *    from the library's own stream-ordered memory pool on `stream`
+ *  - Merges allocate nothing.  The sorts' scratch (their second key and
+ *    value buffers) is taken from the library's own stream-ordered memory
+ *    pool on `stream`
  *    (cudaMallocFromPoolAsync) and freed on the same stream (cudaFreeAsync),
  *    so it is stream-ordered; failure returns OM_ENOMEM.  The pool keeps
  *    freed scratch mapped for later calls, so a device holds up to the
@@ -81,8 +82,9 @@ om_status om_corank_i32_batch(const int64_t *ks, int64_t count,
 
 /*
  * C[0 .. m+n) = stable merge of int32 A[0..m) and B[0..n); ties take A
- * first.  Launches the partition kernel (one co-rank per output range) and
- * the circular-buffer tile-merge kernel on `stream`.
+ * first.  One launch of the circular-buffer tile-merge kernel on `stream`:
+ * each CTA first finds the co-ranks of its output range's two ends (a
+ * search by the whole CTA), then merges the range.  Allocates nothing.
  */
 om_status om_merge_i32(const int32_t *A, int64_t m, const int32_t *B,
                        int64_t n, int32_t *C, void *stream);
@@ -148,13 +150,16 @@ uint64_t om_launch_count(void);
 /*
  * The pages have no counterpart to this call: it is a library convenience.
  *
- * Same result and kernels as om_merge_i32, but it allocates nothing: the
- * co-rank splitters go to a fixed 64 KiB array that the library keeps in
- * device memory (a file-scope __device__ object, held on every GPU that loads
- * the library until the process exits).  For callers that cannot allocate
- * device memory on the call path: processes whose device memory is reserved
- * in full by another allocator, so that a stream-ordered allocation could
- * fail, and code with latency bounds that must not enter an allocator.
+ * Same result as om_merge_i32, in two launches that allocate nothing: the
+ * partition kernel writes one co-rank splitter per output range to a fixed
+ * 64 KiB array that the library keeps in device memory (a file-scope
+ * __device__ object, held on every GPU that loads the library until the
+ * process exits), and the tile-merge kernel reads them.  (om_merge_i32 now
+ * lets each tile-merge CTA find its own splitters, so it allocates nothing
+ * either; this call keeps the two-kernel form.)  For callers that cannot
+ * allocate device memory on the call path: processes whose device memory is
+ * reserved in full by another allocator, and code with latency bounds that
+ * must not enter an allocator.
  *
  *  - m + n may be at most 1,006,510,080 (the array holds 8191 output-range
  *    splitters; ranges are lengthened as needed to fit); larger merges return
@@ -194,8 +199,8 @@ typedef enum {
 /*
  * C[0 .. m+n) = stable merge of the keys A[0..m) and B[0..n) of type
  * `key_type`, both sorted in `order`; ties take A first in either order.
- * The same partition and tile-merge kernels as om_merge_i32, for another
- * element size and comparison.  ("merge_path.cu" runs the method on float
+ * The same tile-merge kernel as om_merge_i32, for another element size and
+ * comparison.  ("merge_path.cu" runs the method on float
  * keys; the co-rank test of "Co-rank Function 實作與 Basic Parallel Merge
  * Kernel", §Important, with <= and < read in the merge order.)
  *  - Floating-point keys compare by value: -0.0 and +0.0 are equal (so the

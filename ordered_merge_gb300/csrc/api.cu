@@ -325,9 +325,10 @@ om_status om_release_scratch(void) {
 
 // ------------------------------------------------- merge without allocating --
 //
-// om_merge_i32_noalloc: the same partition + tile-merge kernels as
-// om_merge_i32, but the splitter scratch lives in the fixed array below
-// instead of coming from cudaMallocAsync.  It exists for callers that must
+// om_merge_i32_noalloc: the merge in its two-kernel form -- the partition
+// kernel writes one co-rank splitter per output range into the fixed array
+// below and the tile-merge kernel reads them (om_merge_i32 instead lets each
+// tile-merge CTA find its own range boundaries).  It exists for callers that must
 // not allocate device memory on the call path: a process whose device memory
 // is already reserved in full by another allocator (a framework's caching
 // allocator, a fixed arena), where a stream-ordered allocation could fail for

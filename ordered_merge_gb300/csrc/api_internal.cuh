@@ -133,23 +133,27 @@ inline om_status cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocatio
 // Sub-tiles per CTA output range (see its definition).
 int64_t subtiles_per_range(int64_t subtiles, int64_t resident_ctas);
 
-// Partition + tile-merge launches for one geometry (split has nranges + 1
-// slots of scratch).
+// The launches of one merge geometry.  split == nullptr: one tile-merge
+// launch whose CTAs find their own range boundaries.  Otherwise split has
+// nranges + 1 slots: the partition kernel fills them, then the tile merge
+// reads them.
 template <typename K, bool V, bool DESC = false>
 cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const DeviceState* d, cudaStream_t st) {
     using Cfg = typename CfgFor<K, V>::type;
     using Smem = SmemFor<K, V>;
-    const unsigned pgrid = (unsigned)((g.nranges + 3) / 4);  // one warp per range
-    cudaError_t e =
-        traced(kKindPartition, st, [&] { partition_kernel<K, V, DESC><<<pgrid, 128, 0, st>>>(g, split); });
-    if (e != cudaSuccess) return e;
+    if (split != nullptr) {
+        const unsigned pgrid = (unsigned)((g.nranges + 3) / 4);  // one warp per range
+        const cudaError_t e =
+            traced(kKindPartition, st, [&] { partition_kernel<K, V, DESC><<<pgrid, 128, 0, st>>>(g, split); });
+        if (e != cudaSuccess) return e;
+    }
     return traced(kKindTileMerge, st, [&] {
         tile_merge_kernel<Cfg, K, V, DESC><<<(unsigned)g.nranges, Cfg::THREADS, Smem::total, st>>>(g, split, d->err);
     });
 }
 
-// One merge of A[0..m) and B[0..n) into C (values optional): splitter
-// scratch from the stream-ordered allocator, then partition + tile merge.
+// One merge of A[0..m) and B[0..n) into C (values optional): one tile-merge
+// launch whose CTAs find their own co-ranks; nothing is allocated.
 // `resident_per_sm`: tile-merge CTAs of this instantiation resident per SM.
 template <typename K, bool V, bool DESC = false>
 om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, const uint32_t* bv, int64_t n, K* ck,
@@ -165,23 +169,15 @@ om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, co
     const int64_t nranges = (total + range_len - 1) / range_len;
     if (nranges > 0x7fffffff) return OM_ERANGE;
     MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
-    int64_t* split = nullptr;
-    cudaError_t e = scratch_alloc(d, reinterpret_cast<void**>(&split), (size_t)(nranges + 1) * 8, st);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return OM_ENOMEM;
-    }
-    e = launch_merge<K, V, DESC>(g, split, d, st);
-    cudaError_t ef = scratch_free(split, st);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return ef == cudaSuccess ? OM_OK : OM_ECUDA;
+    const cudaError_t e = launch_merge<K, V, DESC>(g, nullptr, d, st);
+    return e == cudaSuccess ? OM_OK : cuda_fail(e);
 }
 
 // Stable merge sort of keys[0..n) in place (values optional), in the
 // order DESC.  Pass schedule: one block pass sorts each 4096-element tile in
 // shared memory (early stages: many small merges per block); then one
-// co-rank-split late pass per doubling of the run length, each a partition +
-// tile merge over all pairs of runs.  `resident_per_sm`: tile-merge CTAs of
+// co-rank-split late pass per doubling of the run length, each one tile-merge
+// launch over all pairs of runs.  `resident_per_sm`: tile-merge CTAs of
 // this instantiation resident per SM.
 template <typename K, bool V, bool DESC = false>
 om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cudaStream_t st) {
@@ -197,23 +193,13 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
     const int64_t subtiles = (n + Cfg::T - 1) / Cfg::T;
     const int64_t resident = (int64_t)d->sm_count * (resident_per_sm > 0 ? resident_per_sm : 1);
     const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
-    // splitter slots for the largest late pass (every pair gets the same
-    // number of ranges, including a short last pair), plus one
-    int64_t max_ranges = 1;
-    for (int64_t r = kEarlyTo; r < n; r *= 2) {
-        const int64_t npairs = (n + 2 * r - 1) / (2 * r);
-        const int64_t rps = (2 * r + range_len - 1) / range_len;
-        if (npairs * rps + 1 > max_ranges) max_ranges = npairs * rps + 1;
-    }
 
     K* tk = nullptr;
     uint32_t* tv = nullptr;
-    int64_t* split = nullptr;
     cudaError_t e = cudaSuccess;
     if (passes > 0) {
         e = scratch_alloc(d, reinterpret_cast<void**>(&tk), (size_t)n * sizeof(K), st);
         if (e == cudaSuccess && V) e = scratch_alloc(d, reinterpret_cast<void**>(&tv), (size_t)n * 4, st);
-        if (e == cudaSuccess) e = scratch_alloc(d, reinterpret_cast<void**>(&split), (size_t)max_ranges * 8, st);
         if (e != cudaSuccess) {
             cudaGetLastError();
             if (tk) scratch_free(tk, st);
@@ -241,14 +227,15 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
     }
     for (int64_t r = kEarlyTo; e == cudaSuccess && r < n; r *= 2) {
         // late pass: co-rank split of each pair of runs into output ranges
+        // (each CTA finds the boundaries of its own range)
         const int64_t npairs = (n + 2 * r - 1) / (2 * r);
         const int64_t rps = (2 * r + range_len - 1) / range_len;
         MergeGeom<K> g{src_k, src_v, nullptr, nullptr, dst_k, dst_v, n, 0, r, range_len, rps, npairs * rps};
-        if (g.nranges + 1 > max_ranges || g.nranges > 0x7fffffff) {
+        if (g.nranges > 0x7fffffff) {
             e = cudaErrorInvalidValue;
             break;
         }
-        e = launch_merge<K, V, DESC>(g, split, d, st);
+        e = launch_merge<K, V, DESC>(g, nullptr, d, st);
         K* t = src_k;
         src_k = dst_k;
         dst_k = t;
@@ -257,7 +244,6 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
         dst_v = tq;
     }
     if (passes > 0) {
-        scratch_free(split, st);
         scratch_free(tk, st);
         if (V) scratch_free(tv, st);
     }

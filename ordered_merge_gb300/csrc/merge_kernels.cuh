@@ -481,12 +481,18 @@ struct TileSmem {
     // window descriptors: 2 x {ha, hb, wa, wb, teff, partial_a, partial_b, -},
     // a_used[2], redo[2], abort, padding
     static constexpr size_t info_bytes = 2 * 8 * 4 + 8 * 4;
-    static constexpr size_t total = ring_bytes + stage_bytes + bar_bytes + info_bytes;
+    // the range's two co-ranks when the producer warps search them (int64 x 2)
+    static constexpr size_t bound_bytes = 16;
+    static constexpr size_t total = ring_bytes + stage_bytes + bar_bytes + info_bytes + bound_bytes;
 };
 
 // The tile-merge kernel.  CTA r merges output range r of the geometry,
-// C[k0, k1) from A[i0, i1) and B[j0, j1), where i0 / i1 come from the
-// partition kernel, in sub-tiles of T outputs.  It is warp-specialised: NT
+// C[k0, k1) from A[i0, i1) and B[j0, j1), in sub-tiles of T outputs.  i0 and
+// i1 are the co-ranks of k0 and k1: read from `split` when the partition
+// kernel wrote them there, else (split == nullptr) found by the two producer
+// warps at the start, one rank each (corank_warp), so the merge needs no
+// separate launch and no scratch.  Neighbouring CTAs search the rank they
+// share the same way, so their ranges meet exactly.  It is warp-specialised: NT
 // consumer threads merge; two producer threads (lane 0 of two extra warps)
 // own the bulk copies, one per input side.  Per sub-tile s:
 //   producers: wait for the side's window chunks -> publish it (ready[s],
@@ -521,6 +527,8 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
     int* a_used_slot = info + 16;                        // [2]
     int* redo_slot = info + 18;                          // [2]
     volatile int* abort_flag = info + 20;
+    int64_t* bound_slot = reinterpret_cast<int64_t*>(smem + Smem::ring_bytes + Smem::stage_bytes +
+                                                     Smem::bar_bytes + Smem::info_bytes);  // [2]
 
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
@@ -531,12 +539,16 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
     const int64_t k0 = local * g.range_len;
     if (k0 >= len) return;  // whole CTA
     const int64_t k1 = (k0 + g.range_len < len) ? k0 + g.range_len : len;
-    const int64_t i0 = split[r];
-    const int64_t i1 = (k1 == len) ? s.m : split[r + 1];
-    const int64_t j0 = k0 - i0, j1 = k1 - i1;
-    if (i0 < 0 || i1 < i0 || i1 > s.m || j0 < 0 || j1 < j0 || j1 > s.n) {
-        if (tid == 0) atomicOr(err, kErrBadRange);
-        return;  // whole CTA
+    const bool have_split = split != nullptr;
+    int64_t i0 = 0, i1 = 0;
+    if (have_split) {
+        i0 = split[r];
+        i1 = (k1 == len) ? s.m : split[r + 1];
+        const int64_t j0 = k0 - i0, j1 = k1 - i1;
+        if (i0 < 0 || i1 < i0 || i1 > s.m || j0 < 0 || j1 < j0 || j1 > s.n) {
+            if (tid == 0) atomicOr(err, kErrBadRange);
+            return;  // whole CTA
+        }
     }
     const uintptr_t caddr = reinterpret_cast<uintptr_t>(s.ck);
     const int misc = (int)((caddr / E) & (G - 1));
@@ -561,7 +573,29 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         // Lane 0 of each extra warp: the first streams A, the second B, so
         // the two sides' refills and chunk waits run side by side.  The A
         // producer also owns the stage: it bulk-stores it and hands it back.
+        int64_t kend = k1;  // end of the outputs this CTA merges
+        if (!have_split) {
+            // The first producer warp finds co_rank(k0), the second
+            // co_rank(k1); they swap results through shared memory.  Each
+            // result lies in its rank's legal interval; on unsorted input the
+            // two may still cross, and then the range is dropped (the error
+            // word says so) by publishing no sub-tile.
+            const bool first = tid < NT + 32;
+            const int64_t kk = first ? k0 : k1;
+            const int64_t ii = corank_warp<K, DESC>(kk, s.ak, s.m, s.bk, s.n, tid & 31);
+            if ((tid & 31) == 0) bound_slot[first ? 0 : 1] = ii;
+            named_barrier_sync(1, 64);  // the two producer warps
+            i0 = bound_slot[0];
+            i1 = bound_slot[1];
+            if (i1 < i0 || k1 - i1 < k0 - i0) {
+                if (tid == NT) atomicOr(err, kErrBadRange);
+                i0 = i1 = 0;
+                kend = k0;
+            }
+        }
         if ((tid & 31) != 0) return;
+        const int64_t j0 = (kend == k0) ? 0 : k0 - i0;
+        const int64_t j1 = (kend == k0) ? 0 : k1 - i1;
         const bool side_a = tid == NT;
         SideStream S;
         if (side_a) {
@@ -582,7 +616,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         int last_used = -1;             // this side's consumption in the previous sub-tile
         bool force_full = true;         // wait for the whole window (first sub-tile, after a redo)
         for (int it = 0;; ++it) {
-            const int teff = (int)((k1 - kdone) < T ? (k1 - kdone) : T);
+            const int teff = (int)((kend - kdone) < T ? (kend - kdone) : T);
             int* inf = info + 8 * (it & 1);
             if (teff == 0) {  // every sub-tile is merged: tell the consumers to stop
                 if (side_a) inf[4] = 0;
