@@ -213,6 +213,28 @@ class ClockSampler:
         }
 
 
+# --------------------------------------------------------------- L2 flush --
+
+class L2Flusher:
+    """Evicts L2 by writing a buffer twice its size on the current stream."""
+
+    @staticmethod
+    def l2_bytes(device) -> int:
+        import torch
+
+        return int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20))
+
+    def __init__(self, device):
+        import torch
+
+        self.buf = torch.empty(2 * self.l2_bytes(device), dtype=torch.uint8, device=device)
+        self.val = 0
+
+    def __call__(self):
+        self.val = (self.val + 1) & 0xFF
+        self.buf.fill_(self.val)
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_call(wl: str, h: dict):
@@ -318,7 +340,10 @@ def bench_ours(args):
             else:
                 om.merge_sort_keys(keys, vals, key_type=kt, descending=desc)
 
-    # ---- warm-up, then K timed steps
+    # ---- warm-up, then K timed steps.  A workload whose bytes moved per step
+    # fit twice in L2 gets L2 flushed before every step (a write larger than
+    # L2, outside the timed events); larger ones stream back to back.
+    flush = L2Flusher(device) if total * bytes_per_elem < 2 * L2Flusher.l2_bytes(device) else None
     if step is not None:
         for _ in range(args.warmup):
             step()
@@ -330,17 +355,30 @@ def bench_ours(args):
         om.om_trace_reset()
         om.om_trace_enable(True)
         launches0 = om.om_launch_count()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
         with ClockSampler(local) as clk:
-            ev0.record(stream)
-            for _ in range(args.steps):
-                step()
-            ev1.record(stream)
-            torch.cuda.synchronize(device)
+            if flush is None:
+                ev0 = torch.cuda.Event(enable_timing=True)
+                ev1 = torch.cuda.Event(enable_timing=True)
+                ev0.record(stream)
+                for _ in range(args.steps):
+                    step()
+                ev1.record(stream)
+                torch.cuda.synchronize(device)
+                ms = ev0.elapsed_time(ev1)
+            else:
+                pairs = []
+                for _ in range(args.steps):
+                    flush()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    step()
+                    e1.record(stream)
+                    pairs.append((e0, e1))
+                torch.cuda.synchronize(device)
+                ms = sum(a.elapsed_time(b) for a, b in pairs)
         launches = om.om_launch_count() - launches0
         om.om_trace_enable(False)
-        ms = ev0.elapsed_time(ev1)
     else:
         for _ in range(args.warmup):
             sort_once()
@@ -514,8 +552,8 @@ def bench_ours(args):
                 "scale_log2": args.scale_log2,
                 "m": m,
                 "n": n,
-                "l2": "inputs larger than L2 (no flush)" if total * 4 > 2 * 129e6 else
-                      "inputs smaller than L2: back-to-back steps may hit L2",
+                "l2": "inputs larger than L2 (no flush)" if flush is None else
+                      "L2 flushed before every timed step (a write of 2x L2, outside the timed events)",
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
             "achieved_gbs": round(units_per_step * bytes_per_elem * args.steps
@@ -531,6 +569,82 @@ def bench_ours(args):
             line["pct_of_hbm_peak"] = round(100.0 * line["achieved_gbs"] / peak, 2)
         print(json.dumps(line), flush=True)
     barrier(world, device)
+
+
+# ------------------------------------------------- comparison merges --
+
+def bench_baselines(args):
+    """The unstaged merges the pages measure (one device thread; one thread
+    per slice of 1, 4, 16, 64, 256 outputs with a co-rank search each, no
+    shared memory) beside om_merge_i32, on an int32 merge workload (default
+    of this mode: evens_odds, the pages' own input).  Each row: 3 warm-ups,
+    then --steps timed calls, L2 flushed before each when the workload fits
+    in L2; every row's output is compared with om_merge_i32's first.  Prints
+    one JSON line."""
+    import torch
+
+    import ordered_merge_gb300 as om
+    import synth
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    wl = args.workload
+    if wl not in ("uniform", "evens_odds", "skewed"):
+        raise SystemExit("--baselines needs an int32 merge workload (evens_odds, uniform, skewed)")
+    d = synth.make_device(wl, device, scale_log2=args.scale_log2)
+    A, B = d["A"], d["B"]
+    total = A.numel() + B.numel()
+    stream = torch.cuda.current_stream(device)
+    flush = L2Flusher(device) if total * 8 < 2 * L2Flusher.l2_bytes(device) else None
+    want = om.merge_i32(A, B)
+    C = torch.empty_like(want)
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        if not torch.equal(C, want):
+            raise RuntimeError("a comparison merge gave a different result")
+        times = []
+        for _ in range(reps):
+            if flush is not None:
+                flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times), min(times)
+
+    rows = []
+    reps = max(3, min(args.steps, 20))
+    if total <= (1 << 23):
+        med, best = timed(lambda: om.merge_i32_one_thread(A, B, C), max(3, reps // 4))
+        rows.append({"kernel": "one device thread", "per_thread": total, "threads": 1, "ms_median": med,
+                     "ms_min": best})
+    for s_ in (1, 4, 16, 64, 256):
+        med, best = timed(lambda: om.merge_i32_slices(A, B, C, per_thread=s_), reps)
+        rows.append({"kernel": "one thread per slice, co-rank in global memory, no shared memory",
+                     "per_thread": s_, "threads": (total + s_ - 1) // s_, "ms_median": med, "ms_min": best})
+    med, best = timed(lambda: om.merge_i32(A, B, C), reps)
+    rows.append({"kernel": "om_merge_i32 (range search + circular-buffer tile merge)", "per_thread": None,
+                 "threads": None, "ms_median": med, "ms_min": best})
+    one = rows[0]["ms_median"] if rows[0]["threads"] == 1 else None
+    for r in rows:
+        r["gbs"] = round(total * 8 / (r["ms_median"] / 1e3) / 1e9, 2)
+        r["vs_one_thread"] = round(one / r["ms_median"], 2) if one else None
+        r["ms_median"] = round(r["ms_median"], 5)
+        r["ms_min"] = round(r["ms_min"], 5)
+    line = {"metric": "comparison of merge kernels on one workload", "unit": "ms per call (median)",
+            "workload": WORKLOADS[wl], "name": wl, "m": A.numel(), "n": B.numel(), "reps": reps,
+            "l2": "flushed before every timed call" if flush is not None else "inputs larger than L2",
+            "gbs_counts": "(m+n) x (4 B read + 4 B written); co-rank reads excluded", "rows": rows}
+    print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------- reference arm --
@@ -605,10 +719,14 @@ def main(argv=None):
                    help="reference arm: CPU seconds the K + W oracle steps should take in total")
     p.add_argument("--scale-log2", type=int, default=0,
                    help="shrink the workload by 2^-s (profiling small cases; 0 = the named size)")
+    p.add_argument("--baselines", action="store_true",
+                   help="time the unstaged comparison merges beside om_merge_i32 (one JSON line)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.baselines:
+        bench_baselines(args)
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_ours(args)

@@ -129,8 +129,9 @@ om_status om_device_error(void *stream, uint32_t *detail);
  * With tracing on, every kernel launch is bracketed by two CUDA events on its
  * stream.  om_trace_read synchronises those events and returns, for kernel
  * kind `kind` (0 = partition, 1 = tile merge, 2 = block sort / small merge,
- * 3 = co-rank batch), the number of launches and their summed duration in
- * milliseconds since the last om_trace_reset.
+ * 3 = co-rank batch, 4 = the comparison merges below), the number of
+ * launches and their summed duration in milliseconds since the last
+ * om_trace_reset.
  */
 om_status om_trace_enable(int on);
 om_status om_trace_reset(void);
@@ -178,6 +179,32 @@ uint64_t om_launch_count(void);
  */
 om_status om_merge_i32_noalloc(const int32_t *A, int64_t m, const int32_t *B,
                                int64_t n, int32_t *C, void *stream);
+
+/* ---- the pages' unstaged merges, for comparison ------------------------- */
+
+/*
+ * The two merges that "merge_path.cu" measures, kept to measure what the
+ * shared-memory ring design buys on this GPU.  Same result as om_merge_i32
+ * (int32, ties take A first); same argument rules and errors.  Not fast paths.
+ *
+ * om_merge_i32_one_thread: the two-pointer merge run by one device thread
+ * (one block of one thread).
+ */
+om_status om_merge_i32_one_thread(const int32_t *A, int64_t m,
+                                  const int32_t *B, int64_t n, int32_t *C,
+                                  void *stream);
+
+/*
+ * om_merge_i32_slices: one thread per slice of per_thread outputs (blocks of
+ * 256 threads); each thread finds its slice's start with one co-rank search
+ * in global memory, then merges the slice straight from global memory, with
+ * no shared memory ("Co-rank Function 實作與 Basic Parallel Merge Kernel",
+ * §Basic Parallel Merge Kernel; "merge_path.cu").  per_thread >= 1, else
+ * OM_EINVAL.
+ */
+om_status om_merge_i32_slices(const int32_t *A, int64_t m, const int32_t *B,
+                              int64_t n, int32_t *C, int64_t per_thread,
+                              void *stream);
 
 /* ---- other key types and descending order ------------------------------ */
 

@@ -21,7 +21,7 @@ from .build import LIB_PATH
 
 OM_OK, OM_EINVAL, OM_ERANGE, OM_ENOMEM, OM_ECUDA, OM_EDEVICE = range(6)
 
-KIND_PARTITION, KIND_TILE_MERGE, KIND_BLOCK_SORT, KIND_CORANK = range(4)
+KIND_PARTITION, KIND_TILE_MERGE, KIND_BLOCK_SORT, KIND_CORANK, KIND_BASELINE = range(5)
 
 # om_key_type codes and their element sizes
 KEY_TYPES = {"i32": (0, 4), "u32": (1, 4), "f32": (2, 4), "i64": (3, 8), "u64": (4, 8), "f64": (5, 8)}
@@ -66,6 +66,10 @@ def _load():
     lib.om_merge_keys.restype = I32
     lib.om_merge_sort_keys.argtypes = [I32, I32, P, P, I64, P]
     lib.om_merge_sort_keys.restype = I32
+    lib.om_merge_i32_one_thread.argtypes = [P, I64, P, I64, P, P]
+    lib.om_merge_i32_one_thread.restype = I32
+    lib.om_merge_i32_slices.argtypes = [P, I64, P, I64, P, I64, P]
+    lib.om_merge_i32_slices.restype = I32
     lib.om_release_scratch.argtypes = []
     lib.om_release_scratch.restype = I32
     lib.om_launch_count.argtypes = []
@@ -219,6 +223,33 @@ def om_merge_sort_keys(keys, vals=None, key_type=None, descending=False, stream=
     return keys, vals
 
 
+def om_merge_i32_one_thread(A, B, C=None, stream=None):
+    """The two-pointer merge in one device thread (comparison only)."""
+    import torch
+
+    if C is None:
+        C = torch.empty(A.numel() + B.numel(), dtype=torch.int32, device=A.device)
+    if C.numel() != A.numel() + B.numel():
+        raise ValueError("C must hold len(A) + len(B) elements")
+    _check(_lib.om_merge_i32_one_thread(_ptr4(A, "A"), A.numel(), _ptr4(B, "B"), B.numel(), _ptr4(C, "C"),
+                                        _stream(stream)), "om_merge_i32_one_thread")
+    return C
+
+
+def om_merge_i32_slices(A, B, C=None, per_thread=1, stream=None):
+    """One thread per slice of `per_thread` outputs, no shared memory
+    (comparison only)."""
+    import torch
+
+    if C is None:
+        C = torch.empty(A.numel() + B.numel(), dtype=torch.int32, device=A.device)
+    if C.numel() != A.numel() + B.numel():
+        raise ValueError("C must hold len(A) + len(B) elements")
+    _check(_lib.om_merge_i32_slices(_ptr4(A, "A"), A.numel(), _ptr4(B, "B"), B.numel(), _ptr4(C, "C"),
+                                    int(per_thread), _stream(stream)), "om_merge_i32_slices")
+    return C
+
+
 def om_merge_pairs_u32(keysA, valsA, keysB, valsB, keysC=None, valsC=None, stream=None):
     """Stable merge of (uint32 key, uint32 value) pairs; keys compared unsigned.
 
@@ -297,6 +328,8 @@ merge_i32 = om_merge_i32
 merge_pairs_u32 = om_merge_pairs_u32
 merge_keys = om_merge_keys
 merge_sort_keys = om_merge_sort_keys
+merge_i32_one_thread = om_merge_i32_one_thread
+merge_i32_slices = om_merge_i32_slices
 merge_sort_u32 = om_merge_sort_u32
 device_error = om_device_error
 release_scratch = om_release_scratch

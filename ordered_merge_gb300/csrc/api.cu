@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "api_internal.cuh"
+#include "baseline_kernels.cuh"
 
 namespace om {
 
@@ -261,6 +262,40 @@ om_status om_merge_sort_u32(uint32_t* keys, uint32_t* vals, int64_t n, void* str
     const om_status s = device_state(&d);
     if (s != OM_OK) return s;
     return sort_impl<uint32_t, false>(keys, nullptr, n, d->resident_merge, (cudaStream_t)stream);
+}
+
+om_status om_merge_i32_one_thread(const int32_t* A, int64_t m, const int32_t* B, int64_t n, int32_t* C,
+                                  void* stream) {
+    if (m < 0 || n < 0) return OM_EINVAL;
+    if (m > INT64_MAX - n) return OM_ERANGE;
+    const int64_t total = m + n;
+    if (total == 0) return OM_OK;
+    if ((m > 0 && A == nullptr) || (n > 0 && B == nullptr) || C == nullptr) return OM_EINVAL;
+    if (misaligned4(A) || misaligned4(B) || misaligned4(C)) return OM_EINVAL;
+    if (overlaps(C, total, A, m) || overlaps(C, total, B, n)) return OM_EINVAL;
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e =
+        traced(kKindBaseline, st, [&] { one_thread_merge_kernel<int32_t><<<1, 1, 0, st>>>(A, m, B, n, C); });
+    return e == cudaSuccess ? OM_OK : OM_ECUDA;
+}
+
+om_status om_merge_i32_slices(const int32_t* A, int64_t m, const int32_t* B, int64_t n, int32_t* C,
+                              int64_t per_thread, void* stream) {
+    if (m < 0 || n < 0 || per_thread < 1) return OM_EINVAL;
+    if (m > INT64_MAX - n) return OM_ERANGE;
+    const int64_t total = m + n;
+    if (total == 0) return OM_OK;
+    if ((m > 0 && A == nullptr) || (n > 0 && B == nullptr) || C == nullptr) return OM_EINVAL;
+    if (misaligned4(A) || misaligned4(B) || misaligned4(C)) return OM_EINVAL;
+    if (overlaps(C, total, A, m) || overlaps(C, total, B, n)) return OM_EINVAL;
+    const int64_t threads = (total + per_thread - 1) / per_thread;
+    const int64_t blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffff) return OM_ERANGE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = traced(kKindBaseline, st, [&] {
+        slice_merge_kernel<int32_t><<<(unsigned)blocks, 256, 0, st>>>(A, m, B, n, C, per_thread);
+    });
+    return e == cudaSuccess ? OM_OK : OM_ECUDA;
 }
 
 const char* om_status_string(int status) {

@@ -62,7 +62,14 @@ using SmemFor = TileSmem<typename CfgFor<K, V>::type, V, KeyGeom<K>::E>;
 using SmallMergeCfg = BlockSortCfg<256, 16>;
 constexpr int kEarlyTo = SmallMergeCfg::TILE;  // runs after the block pass: 4096
 
-enum KernelKind { kKindPartition = 0, kKindTileMerge = 1, kKindBlockSort = 2, kKindCorank = 3, kNumKinds = 4 };
+enum KernelKind {
+    kKindPartition = 0,
+    kKindTileMerge = 1,
+    kKindBlockSort = 2,
+    kKindCorank = 3,
+    kKindBaseline = 4,
+    kNumKinds = 5
+};
 
 // ------------------------------------------------------------ device state --
 

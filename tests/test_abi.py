@@ -118,3 +118,16 @@ def test_merge_sort_keys_host_argument_checks():
     assert L.om_merge_sort_keys(f32, 0, 0x1000, 0x2004, 16, None) == om.OM_EINVAL  # 16-byte phase differs
     assert L.om_merge_sort_keys(f32, 1, 0x1000, 0x1010, 16, None) == om.OM_EINVAL  # overlap
     assert L.om_merge_sort_keys(f32, 0, 0x1000, None, (1 << 40) + 1, None) == om.OM_ERANGE
+
+
+def test_comparison_merges_host_argument_checks():
+    import ordered_merge_gb300 as om
+
+    L = om.lib()
+    assert L.om_merge_i32_slices(0x1000, 4, 0x2000, 4, 0x3000, 0, None) == om.OM_EINVAL   # per_thread < 1
+    assert L.om_merge_i32_slices(0x1000, -1, 0x2000, 4, 0x3000, 4, None) == om.OM_EINVAL
+    assert L.om_merge_i32_slices(None, 0, None, 0, None, 4, None) == om.OM_OK
+    assert L.om_merge_i32_slices(0x1000, 4, 0x2000, 4, 0x1008, 4, None) == om.OM_EINVAL  # overlap
+    assert L.om_merge_i32_one_thread(0x1002, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL  # misaligned
+    assert L.om_merge_i32_one_thread(None, 0, None, 0, None, None) == om.OM_OK
+    assert L.om_merge_i32_one_thread(0x1000, 2**62, 0x2000, 2**62, 0x3000, None) == om.OM_ERANGE
