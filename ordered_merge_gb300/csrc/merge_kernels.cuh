@@ -262,6 +262,11 @@ struct TileCfg {
     static constexpr int NCH_LOG2 = RING_LOG2 - CH_LOG2;
     static constexpr int NCH = 1 << NCH_LOG2;
     static constexpr int STAGE = T + 8;
+    // Each side's ring region is RING slots plus an overhang of OVH slots
+    // that mirrors slots [0, OVH): a head placed at slot x < RING can walk
+    // VT - 1 slots on without wrapping, so the serial merge needs no mask.
+    static constexpr int OVH = 32;
+    static constexpr int RSTRIDE = RING + OVH;  // elements per side region (A, then B)
     // largest power of two <= T: the first step of the fixed-step search
     static constexpr int SEARCH_TOP = (T >= 4096) ? 4096 : (T >= 2048) ? 2048 : (T >= 1024) ? 1024
                                     : (T >= 512) ? 512 : (T >= 256) ? 256 : 128;
@@ -271,6 +276,7 @@ struct TileCfg {
     static_assert(T + CH <= RING, "a window of T plus one chunk must fit in the ring");
     static_assert(CH >= 4 && NCH >= 2, "chunks are whole 16-byte groups");
     static_assert(2 * SEARCH_TOP > T, "the fixed-step search must reach every co-rank");
+    static_assert(OVH >= VT && OVH % 4 == 0 && OVH <= CH, "the overhang covers one serial merge, in 16-byte groups");
 };
 
 // Streaming state of one input side (A or B) of one CTA's output range.
@@ -326,11 +332,19 @@ __device__ __forceinline__ void issue_chunk(SideStream& s, int64_t c, K* ring_k,
     const int64_t cs = c << Cfg::CH_LOG2;
     const int64_t ce = cs + Cfg::CH;
     uint64_t* bar = &bars[(int)(c - s.c_first) & (Cfg::NCH - 1)];
+    // A chunk that lands at slot 0 also fills the overhang (its first OVH
+    // elements again at slot RING), in the same barrier transaction.
+    const bool first_slot = ((uint32_t)cs & Cfg::RMASK) == 0;
     if (cs >= s.u_lo && ce <= s.u_hi && cs >= s.arr_lo4 && ce <= s.arr_hi4) {
         const uint32_t slot = (uint32_t)cs & Cfg::RMASK;
-        mbar_arrive_expect_tx(bar, (uint32_t)Cfg::CH * (uint32_t)E * (V ? 2u : 1u));
+        const uint32_t ovh = first_slot ? (uint32_t)Cfg::OVH : 0u;
+        mbar_arrive_expect_tx(bar, ((uint32_t)Cfg::CH + ovh) * (uint32_t)E * (V ? 2u : 1u));
         bulk_copy_g2s(ring_k + slot, s.base16 + E * cs, Cfg::CH * E, bar, policy);
         if (V) bulk_copy_g2s(ring_v + slot, s.vbase16 + 4 * cs, Cfg::CH * 4, bar, policy);
+        if (first_slot) {
+            bulk_copy_g2s(ring_k + Cfg::RING, s.base16 + E * cs, Cfg::OVH * E, bar, policy);
+            if (V) bulk_copy_g2s(ring_v + Cfg::RING, s.vbase16 + 4 * cs, Cfg::OVH * 4, bar, policy);
+        }
         return;
     }
     const int64_t s0 = cs > s.u_lo ? cs : s.u_lo;
@@ -350,21 +364,40 @@ __device__ __forceinline__ void issue_chunk(SideStream& s, int64_t c, K* ring_k,
         bytes = (uint32_t)(be - bs) * (uint32_t)E;
     }
     for (int64_t u = p0; u < p1; ++u) {
-        ring_k[(uint32_t)u & Cfg::RMASK] = gk[u];
-        if (V) ring_v[(uint32_t)u & Cfg::RMASK] = gv[u];
+        const uint32_t slot = (uint32_t)u & Cfg::RMASK;
+        ring_k[slot] = gk[u];
+        if (V) ring_v[slot] = gv[u];
+        if (slot < (uint32_t)Cfg::OVH) {
+            ring_k[Cfg::RING + slot] = gk[u];
+            if (V) ring_v[Cfg::RING + slot] = gv[u];
+        }
         plain = true;
     }
     for (int64_t u = q0; u < q1; ++u) {
-        ring_k[(uint32_t)u & Cfg::RMASK] = gk[u];
-        if (V) ring_v[(uint32_t)u & Cfg::RMASK] = gv[u];
+        const uint32_t slot = (uint32_t)u & Cfg::RMASK;
+        ring_k[slot] = gk[u];
+        if (V) ring_v[slot] = gv[u];
+        if (slot < (uint32_t)Cfg::OVH) {
+            ring_k[Cfg::RING + slot] = gk[u];
+            if (V) ring_v[Cfg::RING + slot] = gv[u];
+        }
         plain = true;
     }
+    // the bulk body's part inside the first OVH elements of a slot-0 chunk
+    int64_t ms = bs > cs ? bs : cs;
+    int64_t me = be < cs + Cfg::OVH ? be : cs + Cfg::OVH;
+    const uint32_t mirror = (first_slot && bytes && me > ms) ? (uint32_t)(me - ms) * (uint32_t)E : 0u;
     if (plain) fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, V ? 2 * bytes : bytes);
+    mbar_arrive_expect_tx(bar, V ? 2 * (bytes + mirror) : bytes + mirror);
     if (bytes) {
         const uint32_t slot = (uint32_t)bs & Cfg::RMASK;
         bulk_copy_g2s(ring_k + slot, s.base16 + E * bs, bytes, bar, policy);
         if (V) bulk_copy_g2s(ring_v + slot, s.vbase16 + 4 * bs, bytes, bar, policy);
+    }
+    if (mirror) {
+        const uint32_t slot = (uint32_t)(ms - cs);
+        bulk_copy_g2s(ring_k + Cfg::RING + slot, s.base16 + E * ms, mirror, bar, policy);
+        if (V) bulk_copy_g2s(ring_v + Cfg::RING + slot, s.vbase16 + 4 * ms, mirror, bar, policy);
     }
 }
 
@@ -394,7 +427,7 @@ __device__ __forceinline__ bool wait_window(SideStream& s, int64_t need_end, uin
 }
 
 // co_rank(d) of the two ring windows, A = ring[(ha + x) & mask] and
-// B = ring[RING | ((hb + x) & mask)]: the largest i in [lo, hi] with i == lo
+// B = ring[RSTRIDE + ((hb + x) & mask)]: the largest i in [lo, hi] with i == lo
 // or A[i-1] <= B[d-i] (in the merge order), by a fixed sequence of
 // power-of-two steps (no data dependent trip count, so a warp never diverges
 // on it).
@@ -405,7 +438,7 @@ __device__ __forceinline__ int corank_ring(int d, int lo, int hi, const K* ring,
         const int cand = lo + step;
         if (cand <= hi) {
             const K x = ring[(ha + (uint32_t)(cand - 1)) & Cfg::RMASK];
-            const K y = ring[Cfg::RING | ((hb + (uint32_t)(d - cand)) & Cfg::RMASK)];
+            const K y = ring[Cfg::RSTRIDE + ((hb + (uint32_t)(d - cand)) & Cfg::RMASK)];
             if (a_first<DESC>(x, y)) lo = cand;
         }
     }
@@ -413,55 +446,65 @@ __device__ __forceinline__ int corank_ring(int d, int lo, int hi, const K* ring,
 }
 
 // Serial merge of VT outputs from the split (a, b) of the two windows, with
-// selects instead of branches: take A unless B's head is strictly smaller
-// (ties go to A).  GUARD adds the exhaustion tests needed when a window ends
-// before the sub-tile does (the last sub-tile of a range); without GUARD all
-// VT steps run.  Returns the A position after the last step.
+// selects instead of branches: take A unless B's head comes strictly before
+// it (ties go to A).  GUARD adds the exhaustion tests needed when a window
+// ends before the sub-tile does (the last sub-tile of a range); without GUARD
+// all VT steps run.  The heads walk linearly through their side's region (the
+// overhang covers the wrap) as byte offsets, and only A's is kept: after v
+// steps B's head is at pa0 + pb0 + v * E - pa.  Returns the A position after
+// the last step.
 template <typename Cfg, typename K, bool V, bool GUARD, bool DESC = false>
 __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, int wb, const K* ring,
                                                  const uint32_t* vring, uint32_t ha, uint32_t hb, K (&keys)[Cfg::VT],
                                                  uint32_t (&vals)[Cfg::VT]) {
     constexpr uint32_t M = Cfg::RMASK;
-    uint32_t ai = ha + (uint32_t)a;
-    uint32_t bi = hb + (uint32_t)b;
-    const uint32_t a_end = ha + (uint32_t)wa;
-    const uint32_t b_end = hb + (uint32_t)wb;
-    const uint32_t ia = ai & M, ib = Cfg::RING | (bi & M);
-    K ak = ring[ia];
-    K bk = ring[ib];
+    constexpr uint32_t E = sizeof(K);
+    static_assert(!V || E == 4, "values share the keys' byte offsets");
+    const char* rk = reinterpret_cast<const char*>(ring);
+    const char* rv = reinterpret_cast<const char*>(vring);
+    const uint32_t pa0 = ((ha + (uint32_t)a) & M) * E;
+    const uint32_t pb0 = ((uint32_t)Cfg::RSTRIDE + ((hb + (uint32_t)b) & M)) * E;
+    const uint32_t sum0 = pa0 + pb0;
+    const uint32_t pa_end = pa0 + (uint32_t)(wa - a) * E;
+    const uint32_t pb_end = pb0 + (uint32_t)(wb - b) * E;
+    uint32_t pa = pa0;
+    K ak = *reinterpret_cast<const K*>(rk + pa0);
+    K bk = *reinterpret_cast<const K*>(rk + pb0);
     // compare forms of the two heads, each computed once when its key is read
     auto ao = OrderKey<K>::of(ak);
     auto bo = OrderKey<K>::of(bk);
     uint32_t av = 0, bv = 0;
     if (V) {
-        av = vring[ia];
-        bv = vring[ib];
+        av = *reinterpret_cast<const uint32_t*>(rv + pa0);
+        bv = *reinterpret_cast<const uint32_t*>(rv + pb0);
     }
 #pragma unroll
     for (int v = 0; v < Cfg::VT; ++v) {
         if (!GUARD || v < cnt) {
-            const bool p = GUARD ? ((bi >= b_end) || ((ai < a_end) && ord_first<DESC>(ao, bo))) : ord_first<DESC>(ao, bo);
+            const uint32_t pb = sum0 + (uint32_t)v * E - pa;
+            const bool p = GUARD ? ((pb >= pb_end) || ((pa < pa_end) && ord_first<DESC>(ao, bo)))
+                                 : ord_first<DESC>(ao, bo);
             keys[v] = p ? ak : bk;
             if (V) vals[v] = p ? av : bv;
-            ai += p ? 1u : 0u;
-            bi += p ? 0u : 1u;
+            const uint32_t pa_next = pa + E;
+            const uint32_t off = p ? pa_next : pb + E;  // the next head of the side just taken
+            pa = p ? pa_next : pa;
             if (v + 1 < Cfg::VT) {
-                const uint32_t idx = p ? (ai & M) : (Cfg::RING | (bi & M));
-                const K nk = ring[idx];
+                const K nk = *reinterpret_cast<const K*>(rk + off);
                 const auto no = OrderKey<K>::of(nk);
                 ak = p ? nk : ak;
                 bk = p ? bk : nk;
                 ao = p ? no : ao;
                 bo = p ? bo : no;
                 if (V) {
-                    const uint32_t nv = vring[idx];
+                    const uint32_t nv = *reinterpret_cast<const uint32_t*>(rv + off);
                     av = p ? nv : av;
                     bv = p ? bv : nv;
                 }
             }
         }
     }
-    return ai - ha;
+    return (uint32_t)a + (pa - pa0) / E;
 }
 
 // A producer publishes a window cut to the data that has already landed when
@@ -474,7 +517,7 @@ constexpr int kPartialMargin = 128;
 // producer/consumer barriers and the per-sub-tile window descriptors.
 template <typename Cfg, bool V, int E = 4>
 struct TileSmem {
-    static constexpr size_t ring_bytes = (size_t)2 * Cfg::RING * (E + (V ? 4 : 0));
+    static constexpr size_t ring_bytes = (size_t)2 * Cfg::RSTRIDE * (E + (V ? 4 : 0));
     static constexpr size_t stage_bytes = (size_t)Cfg::STAGE * (E + (V ? 4 : 0));
     // chunk barriers of A and B, ready[2], done[2], stage_free
     static constexpr size_t bar_bytes = (size_t)(2 * Cfg::NCH + 5) * 8;
@@ -515,7 +558,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
 
     extern __shared__ __align__(128) unsigned char smem[];
     K* ring = reinterpret_cast<K*>(smem);
-    uint32_t* vring = V ? reinterpret_cast<uint32_t*>(ring + 2 * Cfg::RING) : nullptr;
+    uint32_t* vring = V ? reinterpret_cast<uint32_t*>(ring + 2 * Cfg::RSTRIDE) : nullptr;
     K* stage_k = reinterpret_cast<K*>(smem + Smem::ring_bytes);
     uint32_t* stage_v = V ? reinterpret_cast<uint32_t*>(stage_k + Cfg::STAGE) : nullptr;
     uint64_t* bars_a = reinterpret_cast<uint64_t*>(smem + Smem::ring_bytes + Smem::stage_bytes);
@@ -603,8 +646,8 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         } else {
             side_init<Cfg, K>(S, s.bk, s.bv, s.n, j0, j1);
         }
-        K* rk = side_a ? ring : ring + Cfg::RING;
-        uint32_t* rv = V ? (side_a ? vring : vring + Cfg::RING) : nullptr;
+        K* rk = side_a ? ring : ring + Cfg::RSTRIDE;
+        uint32_t* rv = V ? (side_a ? vring : vring + Cfg::RSTRIDE) : nullptr;
         uint64_t* bars = side_a ? bars_a : bars_b;
         char* cbase16 = reinterpret_cast<char*>(caddr & ~uintptr_t(15));
         char* cvbase16 = V ? reinterpret_cast<char*>(reinterpret_cast<uintptr_t>(s.cv) & ~uintptr_t(15)) : nullptr;
