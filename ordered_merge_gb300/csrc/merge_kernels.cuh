@@ -430,19 +430,28 @@ __device__ __forceinline__ bool wait_window(SideStream& s, int64_t need_end, uin
 // B = ring[RSTRIDE + ((hb + x) & mask)]: the largest i in [lo, hi] with i == lo
 // or A[i-1] <= B[d-i] (in the merge order), by a fixed sequence of
 // power-of-two steps (no data dependent trip count, so a warp never diverges
-// on it).
+// on it).  Offsets are kept in bytes, so each probe is two adds, two masks
+// and two loads.
 template <typename Cfg, typename K, bool DESC = false>
 __device__ __forceinline__ int corank_ring(int d, int lo, int hi, const K* ring, uint32_t ha, uint32_t hb) {
+    constexpr uint32_t E = sizeof(K);
+    constexpr uint32_t MB = (uint32_t)Cfg::RING * E - 1;  // byte mask of one ring
+    const char* rk = reinterpret_cast<const char*>(ring);
+    const char* rb = rk + (size_t)Cfg::RSTRIDE * E;       // B region
+    const uint32_t xa = ha * E - E;                      // + cand*E: byte of A[cand-1]
+    const uint32_t xb = (hb + (uint32_t)d) * E;          // - cand*E: byte of B[d-cand]
+    const uint32_t hiE = (uint32_t)hi * E;
+    uint32_t loE = (uint32_t)lo * E;
 #pragma unroll
     for (int step = Cfg::SEARCH_TOP; step > 0; step >>= 1) {
-        const int cand = lo + step;
-        if (cand <= hi) {
-            const K x = ring[(ha + (uint32_t)(cand - 1)) & Cfg::RMASK];
-            const K y = ring[Cfg::RSTRIDE + ((hb + (uint32_t)(d - cand)) & Cfg::RMASK)];
-            if (a_first<DESC>(x, y)) lo = cand;
+        const uint32_t candE = loE + (uint32_t)step * E;
+        if (candE <= hiE) {
+            const K x = *reinterpret_cast<const K*>(rk + ((xa + candE) & MB));
+            const K y = *reinterpret_cast<const K*>(rb + ((xb - candE) & MB));
+            if (a_first<DESC>(x, y)) loE = candE;
         }
     }
-    return lo;
+    return (int)(loE / E);
 }
 
 // Serial merge of VT outputs from the split (a, b) of the two windows, with
