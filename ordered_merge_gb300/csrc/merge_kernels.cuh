@@ -531,7 +531,7 @@ struct TileSmem {
     // chunk barriers of A and B, ready[2], done[2], stage_free
     static constexpr size_t bar_bytes = (size_t)(2 * Cfg::NCH + 5) * 8;
     // window descriptors: 2 x {ha, hb, wa, wb, teff, partial_a, partial_b, -},
-    // a_used[2], redo[2], abort, padding
+    // then the abort flag and padding
     static constexpr size_t info_bytes = 2 * 8 * 4 + 8 * 4;
     // the range's two co-ranks when the producer warps search them (int64 x 2)
     static constexpr size_t bound_bytes = 16;
@@ -547,14 +547,18 @@ struct TileSmem {
 // share the same way, so their ranges meet exactly.  It is warp-specialised: NT
 // consumer threads merge; two producer threads (lane 0 of two extra warps)
 // own the bulk copies, one per input side.  Per sub-tile s:
-//   producers: wait for the side's window chunks -> publish it (ready[s],
-//             count 2) -> wait for the consumers (done[s]) -> advance the
-//             side's head by the sub-tile's co-rank, request freed chunks;
-//             the A producer also bulk-stores the stage and, once that store
-//             has read it, releases it (stage_free)
+//   producers: (window s is published) the A producer releases the stage
+//             once the store of s-1 has read it (stage_free) -> find the
+//             sub-tile's co-rank r on the two windows -> publish window s+1
+//             from data already requested, when it serves (ready[s+1],
+//             count 2) -> wait for the consumers (done[s]) -> advance the side's head by
+//             its share of r, request freed chunks; the A producer
+//             bulk-stores the stage -> publish window s+1 now if it could not
+//             be published early
 //   consumers: wait ready[s] -> co-rank + serial merge -> wait stage_free
 //             (s-1) -> write the stage -> arrive done[s]
-// Consumers never run a CTA-wide barrier and keep no streaming state.
+// Consumers never run a CTA-wide barrier and keep no streaming state; with
+// the next window published while they merge, they rarely wait for it.
 template <typename Cfg, typename K, bool V, bool DESC = false>
 __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g,
                                                                     const int64_t* __restrict__ split,
@@ -576,8 +580,6 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
     uint64_t* done = ready + 2;          // [2]
     uint64_t* stage_free = done + 2;     // [1]
     int* info = reinterpret_cast<int*>(stage_free + 1);  // [2][8]: ha, hb, wa, wb, teff, partial a/b
-    int* a_used_slot = info + 16;                        // [2]
-    int* redo_slot = info + 18;                          // [2]
     volatile int* abort_flag = info + 20;
     int64_t* bound_slot = reinterpret_cast<int64_t*>(smem + Smem::ring_bytes + Smem::stage_bytes +
                                                      Smem::bar_bytes + Smem::info_bytes);  // [2]
@@ -612,8 +614,8 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         }
         mbar_init(&ready[0], 2);  // both producers
         mbar_init(&ready[1], 2);
-        mbar_init(&done[0], NT + 1);  // consumers and the A producer
-        mbar_init(&done[1], NT + 1);
+        mbar_init(&done[0], NT);  // the consumers
+        mbar_init(&done[1], NT);
         mbar_init(stage_free, 1);
         fence_barrier_init();
         *abort_flag = 0;
@@ -665,73 +667,95 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         int64_t kdone = k0;
         bool failed = false;
         int64_t first_new = S.c_first;  // chunks from here on were requested by the latest refill
-        int last_used = -1;             // this side's consumption in the previous sub-tile
-        bool force_full = true;         // wait for the whole window (first sub-tile, after a redo)
-        for (int it = 0;; ++it) {
-            const int teff = (int)((kend - kdone) < T ? (kend - kdone) : T);
+
+        // Publish this side's window of the sub-tile merged in iteration `it`
+        // (outputs from kd; this side's data from head).  A whole window
+        // covers min(T, rest of the range) elements.  A cut window covers only
+        // the part requested before `avail_chunk` (landed by now or soon):
+        // used when it still holds `prev_used` (this side's use in the sub-tile
+        // before) plus a margin, and checked for exactness by both producers
+        // before the sub-tile counts.  early: publishing before the previous
+        // sub-tile's consumers are done, from data already requested; returns
+        // 0 when that data cannot serve, 1 when published, -1 on a timeout.
+        auto publish = [&](int it, int64_t kd, int64_t head, int64_t avail_chunk, int prev_used, bool force_full,
+                           bool early) -> int {
+            const int teff = (int)((kend - kd) < T ? (kend - kd) : T);
             int* inf = info + 8 * (it & 1);
             if (teff == 0) {  // every sub-tile is merged: tell the consumers to stop
                 if (side_a) inf[4] = 0;
                 mbar_arrive(&ready[it & 1]);
-                break;
+                return 1;
             }
-            const int need = (int)((S.u_hi - S.head) < T ? (S.u_hi - S.head) : T);
-            // Part of the window requested before the latest refill (landed by
-            // now); enough when last sub-tile's use of this side, plus a
-            // margin, fits in it.  Publishing it spares the consumers the
-            // DRAM latency of the chunks just requested.
-            const int64_t old_end = (first_new << Cfg::CH_LOG2) < S.u_hi ? (first_new << Cfg::CH_LOG2) : S.u_hi;
-            const int landed = (int)(old_end - S.head < need ? old_end - S.head : need);
+            const int need = (int)((S.u_hi - head) < T ? (S.u_hi - head) : T);
+            const int64_t avail_end = (avail_chunk << Cfg::CH_LOG2) < S.u_hi ? (avail_chunk << Cfg::CH_LOG2) : S.u_hi;
+            const int landed = (int)(avail_end - head < need ? avail_end - head : need);
             int w = need;
             int partial = 0;
-            if (!force_full && teff == T && landed < need && last_used >= 0 &&
-                last_used + kPartialMargin <= landed) {
-                w = landed;
-                partial = 1;
+            const bool can_cut = !force_full && teff == T && prev_used >= 0 && prev_used + kPartialMargin <= landed;
+            if (landed < need) {
+                if (can_cut) {
+                    w = landed;
+                    partial = 1;
+                } else if (early) {
+                    return 0;
+                }
             }
-            const bool ok = wait_window<Cfg>(S, S.head + w, bars, err);
-            inf[side_a ? 0 : 1] = (int)((uint32_t)S.head & Cfg::RMASK);
+            const bool ok = wait_window<Cfg>(S, head + w, bars, err);
+            inf[side_a ? 0 : 1] = (int)((uint32_t)head & Cfg::RMASK);
             inf[side_a ? 2 : 3] = w;
             inf[side_a ? 5 : 6] = partial;
             if (side_a) inf[4] = teff;
             if (!ok) *abort_flag = 1;
             mbar_arrive(&ready[it & 1]);  // release: this side's window and descriptor
-            if (side_a) {
-                if (it > 0) {
-                    bulk_wait_read_all();  // the previous sub-tile's store has read the stage
-                    mbar_arrive(stage_free);
-                }
-                // With both windows published, decide whether a cut window
-                // gives an exact sub-tile: its co-rank r on the windows must
-                // have r < wa and T - r < wb, so that every output's two heads
-                // lie inside them (r is then the true co-rank).  Runs while
-                // the consumers merge.
-                int redo = 0;
-                bool ok2 = mbar_wait_bounded(&ready[it & 1], (uint32_t)(it >> 1) & 1u, err);
-                if (ok2 && (inf[5] | inf[6])) {
-                    const int wa_ = inf[2], wb_ = inf[3];
-                    const int r = corank_ring<Cfg, K, DESC>(teff, teff - wb_ > 0 ? teff - wb_ : 0, teff < wa_ ? teff : wa_,
-                                                      ring, (uint32_t)inf[0], (uint32_t)inf[1]);
-                    a_used_slot[it & 1] = r;
-                    redo = (r < wa_ && teff - r < wb_) ? 0 : 1;
-                }
-                redo_slot[it & 1] = redo;
-                if (!ok2) *abort_flag = 1;
-                mbar_arrive(&done[it & 1]);  // release: a_used (cut windows) and redo flag
+            return ok ? 1 : -1;
+        };
+
+        if (publish(0, kdone, S.head, S.c_first, -1, true, false) < 0) failed = true;
+        for (int it = 0; !failed; ++it) {
+            // Sub-tile `it` is published; the consumers may be merging it.
+            const int teff = (int)((kend - kdone) < T ? (kend - kdone) : T);
+            if (teff == 0) break;  // the stop mark was published
+            if (side_a && it > 0) {
+                bulk_wait_read_all();  // the previous sub-tile's store has read the stage
+                mbar_arrive(stage_free);
             }
-            if (!ok || !mbar_wait_bounded(&done[it & 1], (uint32_t)(it >> 1) & 1u, err)) {
+            const int* inf = info + 8 * (it & 1);
+            if (!mbar_wait_bounded(&ready[it & 1], (uint32_t)(it >> 1) & 1u, err)) {
                 *abort_flag = 1;
                 failed = true;
                 break;
             }
-            if (redo_slot[it & 1]) {
-                force_full = true;  // same sub-tile again, with whole windows; nothing stored
+            // Both windows are visible: each producer finds the sub-tile's
+            // co-rank r on them itself.  A cut window is exact only when
+            // r < wa and T - r < wb (every output's two heads lie inside the
+            // windows, so r is the true co-rank); otherwise the sub-tile is
+            // merged again with whole windows.  This runs while the consumers
+            // merge.
+            const int wa_ = inf[2], wb_ = inf[3];
+            const int r = corank_ring<Cfg, K, DESC>(teff, teff - wb_ > 0 ? teff - wb_ : 0, teff < wa_ ? teff : wa_,
+                                                    ring, (uint32_t)inf[0], (uint32_t)inf[1]);
+            const bool redo = (inf[5] | inf[6]) && !(r < wa_ && teff - r < wb_);
+            const int used = side_a ? r : teff - r;
+            // Publish the next sub-tile now from what is already requested, so
+            // that the consumers find it ready when they finish this one.
+            int next = 0;
+            if (!redo) {
+                next = publish(it + 1, kdone + teff, S.head + used, S.next_issue, used, false, true);
+                if (next < 0) {
+                    failed = true;
+                    break;
+                }
+            }
+            if (!mbar_wait_bounded(&done[it & 1], (uint32_t)(it >> 1) & 1u, err)) {
+                *abort_flag = 1;
+                failed = true;
+                break;
+            }
+            if (redo) {  // same sub-tile again, with whole windows; nothing stored
+                if (publish(it + 1, kdone, S.head, S.next_issue, -1, true, false) < 0) failed = true;
                 continue;
             }
-            force_full = false;
-            const int a_used = a_used_slot[it & 1];
-            last_used = side_a ? a_used : teff - a_used;
-            S.head += last_used;
+            S.head += used;
             first_new = S.next_issue;
             refill<Cfg, K, V>(S, rk, rv, bars, policy);
             if (side_a) {
@@ -760,6 +784,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
                 bulk_commit();
             }
             kdone += teff;
+            if (next == 0 && publish(it + 1, kdone, S.head, first_new, used, false, false) < 0) failed = true;
         }
         if (failed) {
             // Let every requested chunk land (bounded) before the CTA's shared
@@ -794,10 +819,9 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         uint32_t vals[VT];
         const bool full = (teff == T) && (wa == T) && (wb == T);
         int cnt = VT;
-        uint32_t apos;
         if (full) {
             const int a = corank_ring<Cfg, K, DESC>(d, 0, d, ring, ha, hb);
-            apos = merge_serial<Cfg, K, V, false, DESC>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
+            merge_serial<Cfg, K, V, false, DESC>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
         } else if (partial) {
             // Windows cut to the data that has landed (teff == T).  Searches
             // stay inside them and the merge runs without exhaustion tests;
@@ -806,13 +830,13 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
             const int lo = d - wb > 0 ? d - wb : 0;
             const int hi = d < wa ? d : wa;
             const int a = corank_ring<Cfg, K, DESC>(d, lo, hi, ring, ha, hb);
-            apos = merge_serial<Cfg, K, V, false, DESC>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
+            merge_serial<Cfg, K, V, false, DESC>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
         } else {
             cnt = (teff - d < VT) ? teff - d : VT;
             const int lo = d - wb > 0 ? d - wb : 0;
             const int hi = d < wa ? d : wa;
             const int a = corank_ring<Cfg, K, DESC>(d, lo, hi, ring, ha, hb);
-            apos = merge_serial<Cfg, K, V, true, DESC>(a, d - a, cnt, wa, wb, ring, vring, ha, hb, keys, vals);
+            merge_serial<Cfg, K, V, true, DESC>(a, d - a, cnt, wa, wb, ring, vring, ha, hb, keys, vals);
         }
         if (it > 0 && !mbar_wait_bounded(stage_free, (uint32_t)(it - 1) & 1u, err)) {
             *abort_flag = 1;
@@ -834,8 +858,7 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
             }
         }
         fence_proxy_async_smem();  // stage writes -> visible to the bulk store
-        if (tid == NT - 1 && !partial) a_used_slot[it & 1] = (int)apos;  // = co_rank(teff)
-        mbar_arrive(&done[it & 1]);  // release: stage, a_used, ring reads done
+        mbar_arrive(&done[it & 1]);  // release: stage written, ring reads done
     }
 }
 
