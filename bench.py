@@ -441,10 +441,12 @@ def bench_ours(args):
 
     # ---- end to end through the C-ABI call with host buffers
     # Every step copies its inputs from pinned host memory, merges and copies
-    # the result back to pinned host memory.  Consecutive steps alternate
-    # between two streams and two buffer sets, so one step's device-to-host
-    # copy overlaps the next step's host-to-device copy (separate copy
-    # engines), as a caller streaming merges would run them.
+    # the result back to pinned host memory.  A pipeline of three streams --
+    # host-to-device copies, merges, device-to-host copies -- chained by
+    # events over two buffer sets: each direction's copies run one at a time
+    # on their own stream (no two copies split one direction's bandwidth) and
+    # overlap the other direction's and the merges, as a caller streaming
+    # merges would run them.
     e2e = None
     if wl in ("uniform", "evens_odds", "skewed") and args.e2e_steps > 0:
         nbuf = 2
@@ -456,15 +458,31 @@ def bench_ours(args):
         dA = [torch.empty_like(A) for _ in range(nbuf)]
         dB = [torch.empty_like(B) for _ in range(nbuf)]
         dC = [C] + [torch.empty_like(C) for _ in range(nbuf - 1)]
-        streams = [torch.cuda.Stream(device) for _ in range(nbuf)]
+        s_in, s_merge, s_out = (torch.cuda.Stream(device) for _ in range(3))
+        loaded = [torch.cuda.Event() for _ in range(nbuf)]
+        merged = [torch.cuda.Event() for _ in range(nbuf)]
+        drained = [torch.cuda.Event() for _ in range(nbuf)]
+        for b in range(nbuf):  # every buffer starts free
+            merged[b].record(s_merge)
+            drained[b].record(s_out)
 
         def e2e_step(i):
             b = i % nbuf
-            with torch.cuda.stream(streams[b]):
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(merged[b])  # the merge two steps back has read dA/dB[b]
                 dA[b].copy_(hA, non_blocking=True)
                 dB[b].copy_(hB, non_blocking=True)
+                loaded[b].record(s_in)
+            with torch.cuda.stream(s_merge):
+                s_merge.wait_event(loaded[b])
+                s_merge.wait_event(drained[b])  # the copy-out two steps back has read dC[b]
                 om.merge_i32(dA[b], dB[b], dC[b])
+                merged[b].record(s_merge)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(merged[b])
                 hC[b].copy_(dC[b], non_blocking=True)
+                drained[b].record(s_out)
+        streams = (s_in, s_merge, s_out)
 
         def copy_gbs(dst, src):
             """One copy's rate: best of 3 after a warm-up copy (the first
@@ -508,7 +526,7 @@ def bench_ours(args):
             "d2h_bytes_per_step": total * 4,
             "steps": args.e2e_steps,
             "ms_per_step": e_ms / args.e2e_steps,
-            "streams": nbuf,
+            "streams": "3 (copy in, merge, copy out), 2 buffer sets",
             "h2d_gbs_single_copy": round(h2d_gbs, 1),
             "d2h_gbs_single_copy": round(d2h_gbs, 1),
         }
