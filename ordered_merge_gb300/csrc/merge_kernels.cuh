@@ -614,8 +614,8 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
         }
         mbar_init(&ready[0], 2);  // both producers
         mbar_init(&ready[1], 2);
-        mbar_init(&done[0], NT);  // the consumers
-        mbar_init(&done[1], NT);
+        mbar_init(&done[0], NT + 2);  // the consumers, and both producers once they have read the windows
+        mbar_init(&done[1], NT + 2);
         mbar_init(stage_free, 1);
         fence_barrier_init();
         *abort_flag = 0;
@@ -736,6 +736,10 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
                                                     ring, (uint32_t)inf[0], (uint32_t)inf[1]);
             const bool redo = (inf[5] | inf[6]) && !(r < wa_ && teff - r < wb_);
             const int used = side_a ? r : teff - r;
+            // This producer has read the windows: `done` (which both refills
+            // wait for) may now complete, so no refill overwrites a window
+            // slot that the other producer is still searching.
+            mbar_arrive(&done[it & 1]);
             // Publish the next sub-tile now from what is already requested, so
             // that the consumers find it ready when they finish this one.
             int next = 0;
