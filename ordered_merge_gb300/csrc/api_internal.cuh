@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -193,6 +194,22 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
     DeviceState* d = nullptr;
     om_status s = device_state(&d);
     if (s != OM_OK) return s;
+    {
+        // Once per device: the largest shared-memory carveout, so that the
+        // block pass runs MIN_CTAS tiles per SM.
+        static std::mutex mu;
+        static bool carved[128];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return OM_ECUDA;
+        std::lock_guard<std::mutex> lk(mu);
+        if (!carved[dev]) {
+            if (cudaFuncSetAttribute(block_sort_kernel<SmallMergeCfg, K, V, DESC>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                return OM_ECUDA;
+            carved[dev] = true;
+        }
+    }
 
     int passes = 0;  // global passes after the block pass
     for (int64_t r = kEarlyTo; r < n; r *= 2) ++passes;

@@ -62,13 +62,23 @@ struct BlockSortCfg {
     static constexpr int VT = VT_;
     static constexpr int TILE = NT * VT;
     static constexpr int PADDED = TILE + TILE / 32;
+    // CTAs per SM to hold the registers to (with the shared-memory carveout
+    // set to its maximum, four tiles fit)
+    static constexpr int MIN_CTAS = 4;
     static_assert((VT & (VT - 1)) == 0, "VT must be a power of two");
     static_assert(TILE % 32 == 0, "tile is whole bank rows");
 };
 
+// Padded keys (and values) of one tile, plus one 16-byte group so that a
+// merge may read the element one past the tile's last without a clamp.
+template <typename Cfg, typename K>
+constexpr int block_sort_key_slots() {
+    return Cfg::TILE + Cfg::TILE / (128 / (int)sizeof(K)) + 16 / (int)sizeof(K);
+}
+
 template <typename Cfg, typename K, bool V>
 constexpr size_t block_sort_smem_bytes() {
-    return (size_t)(Cfg::TILE + Cfg::TILE / (128 / sizeof(K))) * sizeof(K) + (V ? (size_t)Cfg::PADDED * 4 : 0);
+    return (size_t)block_sort_key_slots<Cfg, K>() * sizeof(K) + (V ? (size_t)(Cfg::PADDED + 4) * 4 : 0);
 }
 
 // co_rank(d) of A = s[pad(a0 + x)], x < m and B = s[pad(b0 + x)], x < n:
@@ -88,12 +98,12 @@ __device__ __forceinline__ int corank_padded(int d, const K* s, int a0, int m, i
 }
 
 template <typename Cfg, typename K, bool V, bool DESC = false>
-__global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const K* in_k, const uint32_t* in_v, K* out_k,
+__global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_CTAS) block_sort_kernel(const K* in_k, const uint32_t* in_v, K* out_k,
                                                              uint32_t* out_v, int64_t n, int run_from, int run_to) {
     constexpr int NT = Cfg::NT;
     constexpr int VT = Cfg::VT;
     constexpr int TILE = Cfg::TILE;
-    constexpr int PADDED_K = TILE + TILE / (128 / (int)sizeof(K));
+    constexpr int PADDED_K = block_sort_key_slots<Cfg, K>();
     static_assert(!V || sizeof(K) == 4, "values ride with 4-byte keys");
     extern __shared__ __align__(16) unsigned char bsm_raw[];
     K* sk = reinterpret_cast<K*>(bsm_raw);
@@ -163,12 +173,13 @@ __global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const K* in_k, cons
             cnt = (m + nb - d) < VT ? (m + nb - d) : VT;
             const int a = corank_padded<K, DESC>(d, sk, a0, m, b0, nb, w);
             // Serial merge with selects: A and B are adjacent runs, so one
-            // index (clamped into the tile) reaches either head.  Take A
-            // unless A is exhausted or B's head comes strictly before it.
+            // index reaches either head (at most one past the tile's last
+            // element: the spare slot).  Take A unless A is exhausted or B's
+            // head comes strictly before it.
             int ia = a0 + a, ib = b0 + (d - a);
             const int ea = a0 + m, eb = b0 + nb;
-            int x = ia < TILE - 1 ? ia : TILE - 1;
-            int y = ib < TILE - 1 ? ib : TILE - 1;
+            const int x = ia;  // at most TILE: the spare slot
+            const int y = ib;
             K ak = sk[padk<K>(x)], bk = sk[padk<K>(y)];
             auto ao = OrderKey<K>::of(ak);
             auto bo = OrderKey<K>::of(bk);
@@ -182,8 +193,7 @@ __global__ void __launch_bounds__(Cfg::NT) block_sort_kernel(const K* in_k, cons
                     ia += p ? 1 : 0;
                     ib += p ? 0 : 1;
                     if (i + 1 < VT) {
-                        int idx = p ? ia : ib;
-                        idx = idx < TILE - 1 ? idx : TILE - 1;
+                        const int idx = p ? ia : ib;  // at most TILE: the spare slot
                         const K nk = sk[padk<K>(idx)];
                         const auto no = OrderKey<K>::of(nk);
                         ak = p ? nk : ak;

@@ -172,3 +172,20 @@ def test_long_ranges_uneven_consumption(gpu, monkeypatch, per_range, ties):
     A, B = _bursty(rng, 400, ties)
     check(gpu, A, B)
     check(gpu, B, A)
+
+
+@pytest.mark.parametrize("m,n", [(100003, 99991), (5000, 300007), (1, 50000)])
+def test_unsorted_input_terminates_in_bounds(gpu, m, n):
+    """Sortedness is a precondition the library does not check.  On unsorted
+    input the output is unspecified, but every kernel must still end (its
+    searches and waits are bounded) and write nothing outside C; the device
+    error word may report a dropped range, never a timed-out wait."""
+    rng = np.random.default_rng(m + n)
+    A = rng.integers(-1000, 1000, m).astype(np.int32)
+    B = rng.integers(-1000, 1000, n).astype(np.int32)
+    total = m + n
+    buf, C = guarded_empty(total)
+    gpu.merge_i32(dev_i32(A), dev_i32(B), C)
+    torch.cuda.synchronize()
+    assert gpu.device_error() in (0, 2), "a kernel wait timed out on unsorted input"
+    assert guards_intact(buf, total), "merge wrote outside C"
