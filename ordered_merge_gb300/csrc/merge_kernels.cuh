@@ -15,9 +15,11 @@
 //    Model 與 Circular 函式.
 //
 // GB300 design (what differs from the pages):
-//  * The grid-level co-rank is a separate partition kernel that writes one
-//    splitter per output range (instead of thread 0 of every block), each
-//    found by one warp probing 32 points per round (higher radix).
+//  * The block-level co-rank of each CTA's output range is found inside the
+//    tile-merge kernel by its two producer warps, one range end each, each
+//    warp probing 32 points per round (higher radix).  A separate partition
+//    kernel that writes the same splitters to an array serves the entry
+//    point that keeps them in a fixed device array.
 //  * Every search is a bounded form of the same co-rank: the largest i in
 //    [max(0,k-n), min(k,m)] with i == lower bound or A[i-1] <= B[k-i].  On
 //    sorted input it is the pages' i; on any input it stops.
@@ -27,7 +29,10 @@
 //    the pages' "% tile_size" wrap is a mask.
 //  * Refills run ahead: a chunk is requested as soon as the slots it lands
 //    in are consumed, so input for later sub-tiles is in flight while the
-//    current one is merged.
+//    current one is merged; each ring has a 32-slot overhang that mirrors its
+//    first slots, so a serial merge never wraps.
+//  * The producers compute each sub-tile's co-rank themselves and publish
+//    the next sub-tile's window while the consumers merge the current one.
 //  * The kernel is warp-specialised: two producer threads (one per input
 //    side) own all bulk copies and the consumed-count bookkeeping; consumer
 //    warps only search, merge and stage, synchronised with the producers by
@@ -516,8 +521,8 @@ __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, 
     return (uint32_t)a + (pa - pa0) / E;
 }
 
-// A producer publishes a window cut to the data that has already landed when
-// the previous sub-tile's use of its side plus this margin fits in it.
+// A producer publishes a window cut to the data already requested when the
+// previous sub-tile's use of its side plus this margin fits in it.
 constexpr int kPartialMargin = 128;
 
 // Shared memory of the tile-merge kernel: keys of both rings back to back
@@ -827,10 +832,11 @@ __global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g
             const int a = corank_ring<Cfg, K, DESC>(d, 0, d, ring, ha, hb);
             merge_serial<Cfg, K, V, false, DESC>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
         } else if (partial) {
-            // Windows cut to the data that has landed (teff == T).  Searches
-            // stay inside them and the merge runs without exhaustion tests;
-            // the A producer checks that the result is exact and, if not,
-            // the sub-tile is discarded and published again with whole windows.
+            // Windows cut to the data already requested (teff == T).
+            // Searches stay inside them and the merge runs without
+            // exhaustion tests; the producers check that the result is exact
+            // and, if not, the sub-tile is discarded and published again with
+            // whole windows.
             const int lo = d - wb > 0 ? d - wb : 0;
             const int hi = d < wa ? d : wa;
             const int a = corank_ring<Cfg, K, DESC>(d, lo, hi, ring, ha, hb);
