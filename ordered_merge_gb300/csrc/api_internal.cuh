@@ -58,10 +58,11 @@ using SmemFor = TileSmem<typename CfgFor<K, V>::type, V, KeyGeom<K>::E>;
 
 //  sort: one block pass sorts 256 x 16 = 4096-element tiles in shared memory
 //        (runs of 16 in registers, then merges of whole pairs of runs per
-//        CTA through 1024 to 4096); later passes use
-//        the partition + tile-merge kernels on each pair of runs.
+//        CTA up to 4096); later passes use the tile-merge kernel on each
+//        pair of runs.  (8192-element tiles measured even: the extra block
+//        level costs what the removed late pass saved.)
 using SmallMergeCfg = BlockSortCfg<256, 16>;
-constexpr int kEarlyTo = SmallMergeCfg::TILE;  // runs after the block pass: 4096
+constexpr int kEarlyTo = SmallMergeCfg::TILE;  // runs after the block pass
 
 enum KernelKind {
     kKindPartition = 0,
@@ -189,8 +190,6 @@ om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, co
 // this instantiation resident per SM.
 template <typename K, bool V, bool DESC = false>
 om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cudaStream_t st) {
-    static_assert(block_sort_smem_bytes<SmallMergeCfg, K, V>() <= 48 * 1024,
-                  "the block pass fits the default shared-memory limit");
     DeviceState* d = nullptr;
     om_status s = device_state(&d);
     if (s != OM_OK) return s;
@@ -203,9 +202,11 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return OM_ECUDA;
         std::lock_guard<std::mutex> lk(mu);
         if (!carved[dev]) {
-            if (cudaFuncSetAttribute(block_sort_kernel<SmallMergeCfg, K, V, DESC>,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            auto* kern = block_sort_kernel<SmallMergeCfg, K, V, DESC>;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)block_sort_smem_bytes<SmallMergeCfg, K, V>()) != cudaSuccess)
                 return OM_ECUDA;
             carved[dev] = true;
         }

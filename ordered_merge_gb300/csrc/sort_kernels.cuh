@@ -62,9 +62,9 @@ struct BlockSortCfg {
     static constexpr int VT = VT_;
     static constexpr int TILE = NT * VT;
     static constexpr int PADDED = TILE + TILE / 32;
-    // CTAs per SM to hold the registers to (with the shared-memory carveout
-    // set to its maximum, four tiles fit)
-    static constexpr int MIN_CTAS = 4;
+    // CTAs per SM to hold the registers to: 1024 threads' worth (with the
+    // shared-memory carveout set to its maximum, that many tiles fit)
+    static constexpr int MIN_CTAS = NT >= 1024 ? 1 : 1024 / NT;
     static_assert((VT & (VT - 1)) == 0, "VT must be a power of two");
     static_assert(TILE % 32 == 0, "tile is whole bank rows");
 };
