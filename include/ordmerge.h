@@ -146,6 +146,22 @@ om_status om_release_scratch(void);
 /* Number of kernels this library has launched since load. */
 uint64_t om_launch_count(void);
 
+/*
+ * Launch planning, host only (no device call): the number of sub-tiles per
+ * CTA output range the library uses for one tile-merge launch over `segs`
+ * independent merges of at most `seg_len` outputs each (a merge: segs = 1;
+ * a late pass of the sort: one segment per pair of runs), with sub-tiles of
+ * `subtile` outputs, `bytes_per_output` bytes read plus written per output
+ * and `resident_ctas` CTAs running at a time.  Ranges never cross a
+ * segment.  The choice minimises  waves x (fixed cost per range + longest
+ * range)  over one to eight waves, so that no launch ends on a partial wave
+ * of a few CTAs.  The environment variables OM_WAVES (fixed wave count) and
+ * OM_SUBTILES_PER_RANGE (fixed result) override it, here and in every call.
+ * Returns a value >= 1, or 0 when an argument is not positive.
+ */
+int64_t om_subtiles_per_range(int64_t segs, int64_t seg_len, int64_t subtile, int64_t bytes_per_output,
+                              int64_t resident_ctas);
+
 /* ---- merge without allocating ------------------------------------------ */
 
 /*

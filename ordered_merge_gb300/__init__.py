@@ -74,6 +74,8 @@ def _load():
     lib.om_release_scratch.restype = I32
     lib.om_launch_count.argtypes = []
     lib.om_launch_count.restype = ctypes.c_uint64
+    lib.om_subtiles_per_range.argtypes = [I64, I64, I64, I64, I64]
+    lib.om_subtiles_per_range.restype = I64
     return lib
 
 
@@ -320,6 +322,11 @@ def om_release_scratch():
 
 def om_launch_count() -> int:
     return int(_lib.om_launch_count())
+
+
+def om_subtiles_per_range(segs: int, seg_len: int, subtile: int, bytes_per_output: int, resident_ctas: int) -> int:
+    """Sub-tiles per CTA output range the library picks for one launch (host only)."""
+    return int(_lib.om_subtiles_per_range(segs, seg_len, subtile, bytes_per_output, resident_ctas))
 
 
 corank_i32 = om_corank_i32

@@ -147,17 +147,56 @@ static int64_t env_int(const char* name, int64_t fallback) {
     return (end != s && v > 0) ? (int64_t)v : fallback;
 }
 
-// Sub-tiles per CTA output range.  Every range has the same number of
-// outputs, so the merge costs the same in each; the grid is sized to a whole
-// number of waves of resident CTAs (OM_WAVES, default 1) so that no SM idles
-// through a partial last wave.  Long ranges also amortise each CTA's start-up
-// (the latency of its first chunks).  OM_SUBTILES_PER_RANGE overrides.
-int64_t subtiles_per_range(int64_t subtiles, int64_t resident_ctas) {
-    const int64_t waves = env_int("OM_WAVES", 1);
-    const int64_t slots = resident_ctas * waves;
-    int64_t s = (subtiles + slots - 1) / slots;
-    if (s < 1) s = 1;
-    return env_int("OM_SUBTILES_PER_RANGE", s);
+// Sub-tiles per CTA output range for one launch over `segs` independent
+// merges of at most `seg_len` outputs each (a merge: one segment; a late
+// pass of the sort: one segment per pair of runs).  A range never crosses a
+// segment, so each segment splits into ceil(seg_len / L) ranges of
+// L = per_range * T outputs, and resident_ctas of them run at a time.
+//
+// The launch's time is modelled as  waves * (overhead + longest range):
+// a partial last wave costs as much as a full one (a few CTAs left over
+// after a full wave run alone for a whole range), and every range pays a
+// fixed cost, its two co-rank searches in global memory and the latency of
+// its first chunks, about what moving kRangeOverheadBytes costs a CTA at
+// full rate.  Over 1 to 8 waves the rule takes the range length with the
+// least modelled time (ties: fewer waves).  For one segment that is always
+// one full wave of equal ranges; for the sort's middle passes, whose pairs
+// do not divide evenly into the resident CTAs, it is often two to four
+// waves of shorter ranges.  The constant is fitted to the measured late
+// passes of a 2^26-key sort, where this rule picked each pass's fastest
+// measured range length.  OM_WAVES fixes the wave count;
+// OM_SUBTILES_PER_RANGE fixes the result.
+static constexpr int64_t kRangeOverheadBytes = 24576;
+
+int64_t subtiles_per_range(int64_t segs, int64_t seg_len, int64_t T, int64_t bytes_per_output,
+                           int64_t resident_ctas) {
+    const int64_t forced = env_int("OM_SUBTILES_PER_RANGE", 0);
+    if (forced > 0) return forced;
+    if (segs < 1 || seg_len < 1 || T < 1) return 1;
+    const int64_t slots = resident_ctas > 0 ? resident_ctas : 1;
+    const int64_t qmax = (seg_len + T - 1) / T;
+    const int64_t overhead = kRangeOverheadBytes / (bytes_per_output > 0 ? bytes_per_output : 1);
+    const int64_t w_fixed = env_int("OM_WAVES", 0);
+    const int64_t w_lo = w_fixed > 0 ? w_fixed : 1, w_hi = w_fixed > 0 ? w_fixed : 8;
+    auto ranges = [&](int64_t q) { return segs * ((seg_len + q * T - 1) / (q * T)); };
+    int64_t best_q = qmax, best_cost = -1;
+    for (int64_t w = w_lo; w <= w_hi; ++w) {
+        // the shortest ranges that keep the count within w waves
+        int64_t lo = 1, hi = qmax;
+        while (lo < hi) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (ranges(mid) <= w * slots) hi = mid;
+            else lo = mid + 1;
+        }
+        const int64_t len = lo * T < seg_len ? lo * T : seg_len;
+        const int64_t waves = (ranges(lo) + slots - 1) / slots;
+        const int64_t cost = waves * (overhead + len);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_q = lo;
+        }
+    }
+    return best_q;
 }
 
 }  // namespace om
@@ -350,6 +389,12 @@ om_status om_trace_read(int kind, int64_t* launches, double* total_ms) {
 
 uint64_t om_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int64_t om_subtiles_per_range(int64_t segs, int64_t seg_len, int64_t subtile, int64_t bytes_per_output,
+                              int64_t resident_ctas) {
+    if (segs < 1 || seg_len < 1 || subtile < 1 || bytes_per_output < 1 || resident_ctas < 1) return 0;
+    return subtiles_per_range(segs, seg_len, subtile, bytes_per_output, resident_ctas);
+}
+
 om_status om_release_scratch(void) {
     DeviceState* d = nullptr;
     const om_status s = device_state(&d);
@@ -423,7 +468,7 @@ om_status om_merge_i32_noalloc(const int32_t* A, int64_t m, const int32_t* B, in
     if (s != OM_OK) return s;
 
     const int64_t subtiles = (total + MergeCfg::T - 1) / MergeCfg::T;
-    int64_t per_range = subtiles_per_range(subtiles, (int64_t)d->sm_count * d->resident_merge);
+    int64_t per_range = subtiles_per_range(1, total, MergeCfg::T, 8, (int64_t)d->sm_count * d->resident_merge);
     const int64_t fit = (subtiles + kNoAllocSplits - 2) / (kNoAllocSplits - 1);  // ranges must fit the array
     if (per_range < fit) per_range = fit;
     const int64_t range_len = per_range * MergeCfg::T;

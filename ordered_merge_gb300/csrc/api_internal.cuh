@@ -139,8 +139,16 @@ inline bool overlaps(const void* a, int64_t na, const void* b, int64_t nb, int e
 
 inline om_status cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocation ? OM_ENOMEM : OM_ECUDA; }
 
-// Sub-tiles per CTA output range (see its definition).
-int64_t subtiles_per_range(int64_t subtiles, int64_t resident_ctas);
+// Sub-tiles per CTA output range of a launch over `segs` merges of at most
+// `seg_len` outputs, moving bytes_per_output bytes per output, with
+// resident_ctas CTAs at a time (see its definition).
+int64_t subtiles_per_range(int64_t segs, int64_t seg_len, int64_t T, int64_t bytes_per_output,
+                           int64_t resident_ctas);
+
+template <typename K, bool V>
+constexpr int64_t bytes_per_output() {
+    return 2 * ((int64_t)sizeof(K) + (V ? 4 : 0));
+}
 
 // The launches of one merge geometry.  split == nullptr: one tile-merge
 // launch whose CTAs find their own range boundaries.  Otherwise split has
@@ -172,9 +180,8 @@ om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, co
     if (s != OM_OK) return s;
     using Cfg = typename CfgFor<K, V>::type;
     const int64_t total = m + n;
-    const int64_t subtiles = (total + Cfg::T - 1) / Cfg::T;
     const int64_t resident = (int64_t)d->sm_count * (resident_per_sm > 0 ? resident_per_sm : 1);
-    const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
+    const int64_t range_len = subtiles_per_range(1, total, Cfg::T, bytes_per_output<K, V>(), resident) * Cfg::T;
     const int64_t nranges = (total + range_len - 1) / range_len;
     if (nranges > 0x7fffffff) return OM_ERANGE;
     MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
@@ -215,9 +222,7 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
     int passes = 0;  // global passes after the block pass
     for (int64_t r = kEarlyTo; r < n; r *= 2) ++passes;
     using Cfg = typename CfgFor<K, V>::type;
-    const int64_t subtiles = (n + Cfg::T - 1) / Cfg::T;
     const int64_t resident = (int64_t)d->sm_count * (resident_per_sm > 0 ? resident_per_sm : 1);
-    const int64_t range_len = subtiles_per_range(subtiles, resident) * Cfg::T;
 
     K* tk = nullptr;
     uint32_t* tv = nullptr;
@@ -254,6 +259,9 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
         // late pass: co-rank split of each pair of runs into output ranges
         // (each CTA finds the boundaries of its own range)
         const int64_t npairs = (n + 2 * r - 1) / (2 * r);
+        const int64_t seg = 2 * r < n ? 2 * r : n;
+        const int64_t range_len =
+            subtiles_per_range(npairs, seg, Cfg::T, bytes_per_output<K, V>(), resident) * Cfg::T;
         const int64_t rps = (2 * r + range_len - 1) / range_len;
         MergeGeom<K> g{src_k, src_v, nullptr, nullptr, dst_k, dst_v, n, 0, r, range_len, rps, npairs * rps};
         if (g.nranges > 0x7fffffff) {
