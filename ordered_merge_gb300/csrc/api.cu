@@ -475,7 +475,7 @@ om_status om_merge_i32_noalloc(const int32_t* A, int64_t m, const int32_t* B, in
     const int64_t nranges = (total + range_len - 1) / range_len;
     if (nranges + 1 > kNoAllocSplits) return OM_ERANGE;
     MergeGeom<int32_t> g{A, nullptr, B, nullptr, C, nullptr, m, n, 0, range_len, nranges, nranges};
-    const cudaError_t e = launch_merge<int32_t, false>(g, split, d, (cudaStream_t)stream);
+    const cudaError_t e = launch_merge<MergeCfg, int32_t, false>(g, split, d, (cudaStream_t)stream);
     return e == cudaSuccess ? OM_OK : cuda_fail(e);
 }
 

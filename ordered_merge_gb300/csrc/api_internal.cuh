@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda_runtime.h>
 
@@ -29,9 +30,18 @@ using MergeCfg = TileCfg<128, 23, 12, 10>;
 //  rings, 512-element chunks (best of the shapes measured on GB300).
 using PairsCfg = TileCfg<128, 11, 11, 9>;
 //  8-byte keys: the same ring bytes as the key+value merge (two 16 KB rings
-//  of 2048 keys, 4 KB chunks), so the same shape.
-using WideCfg = TileCfg<128, 11, 11, 9>;
+//  of 2048 keys).  A merge takes half the consumers with about twice the
+//  outputs each, so each output pays half a co-rank search: 64 x 23 = 1472
+//  outputs per sub-tile and 2 KB chunks for int64 / uint64 (0.705 -> 0.685 ms
+//  on 2^28 outputs), 64 x 21 = 1344 and 4 KB chunks for float64, whose every
+//  search probe also converts two keys to integers (0.977 -> 0.901 ms).
+//  The sort's late passes ran slower with every 64-consumer shape measured
+//  (2^26 float64 keys: 5.17 against 5.33-5.74 ms), so sorts keep 128 x 11.
+using WideMergeCfg = TileCfg<64, 23, 11, 8>;
+using F64MergeCfg = TileCfg<64, 21, 11, 9>;
+using WideSortCfg = TileCfg<128, 11, 11, 9>;
 
+// Tile shape of a merge of K keys (with values when V).
 template <typename K, bool V>
 struct CfgFor {
     using type = MergeCfg;
@@ -42,19 +52,27 @@ struct CfgFor<K, true> {
 };
 template <>
 struct CfgFor<int64_t, false> {
-    using type = WideCfg;
+    using type = WideMergeCfg;
 };
 template <>
 struct CfgFor<uint64_t, false> {
-    using type = WideCfg;
+    using type = WideMergeCfg;
 };
 template <>
 struct CfgFor<double, false> {
-    using type = WideCfg;
+    using type = F64MergeCfg;
 };
 
+// Tile shape of the sort's late passes.
 template <typename K, bool V>
-using SmemFor = TileSmem<typename CfgFor<K, V>::type, V, KeyGeom<K>::E>;
+struct SortCfgFor {
+    using type = typename std::conditional<sizeof(K) == 8 && !V, WideSortCfg, typename CfgFor<K, V>::type>::type;
+};
+
+template <typename Cfg, typename K, bool V>
+using SmemOf = TileSmem<Cfg, V, KeyGeom<K>::E>;
+template <typename K, bool V>
+using SmemFor = SmemOf<typename CfgFor<K, V>::type, K, V>;
 
 //  sort: one block pass sorts 256 x 16 = 4096-element tiles in shared memory
 //        (runs of 16 in registers, then merges of whole pairs of runs per
@@ -154,10 +172,9 @@ constexpr int64_t bytes_per_output() {
 // launch whose CTAs find their own range boundaries.  Otherwise split has
 // nranges + 1 slots: the partition kernel fills them, then the tile merge
 // reads them.
-template <typename K, bool V, bool DESC = false>
+template <typename Cfg, typename K, bool V, bool DESC = false>
 cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const DeviceState* d, cudaStream_t st) {
-    using Cfg = typename CfgFor<K, V>::type;
-    using Smem = SmemFor<K, V>;
+    using Smem = SmemOf<Cfg, K, V>;
     if (split != nullptr) {
         const unsigned pgrid = (unsigned)((g.nranges + 3) / 4);  // one warp per range
         const cudaError_t e =
@@ -185,7 +202,7 @@ om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, co
     const int64_t nranges = (total + range_len - 1) / range_len;
     if (nranges > 0x7fffffff) return OM_ERANGE;
     MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, range_len, nranges, nranges};
-    const cudaError_t e = launch_merge<K, V, DESC>(g, nullptr, d, st);
+    const cudaError_t e = launch_merge<Cfg, K, V, DESC>(g, nullptr, d, st);
     return e == cudaSuccess ? OM_OK : cuda_fail(e);
 }
 
@@ -221,7 +238,7 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
 
     int passes = 0;  // global passes after the block pass
     for (int64_t r = kEarlyTo; r < n; r *= 2) ++passes;
-    using Cfg = typename CfgFor<K, V>::type;
+    using Cfg = typename SortCfgFor<K, V>::type;
     const int64_t resident = (int64_t)d->sm_count * (resident_per_sm > 0 ? resident_per_sm : 1);
 
     K* tk = nullptr;
@@ -268,7 +285,7 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
             e = cudaErrorInvalidValue;
             break;
         }
-        e = launch_merge<K, V, DESC>(g, nullptr, d, st);
+        e = launch_merge<Cfg, K, V, DESC>(g, nullptr, d, st);
         K* t = src_k;
         src_k = dst_k;
         dst_k = t;

@@ -14,8 +14,8 @@
 namespace om {
 
 // Once per device and instantiation: the shared-memory limit of the
-// tile-merge kernel and how many of its CTAs are resident per SM.
-template <typename K, bool V, bool DESC>
+// tile-merge kernel of shape Cfg and how many of its CTAs are resident per SM.
+template <typename Cfg, typename K, bool V, bool DESC>
 static om_status prepare_typed(int* resident) {
     static std::mutex mu;
     static int cached[128];
@@ -23,8 +23,7 @@ static om_status prepare_typed(int* resident) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return OM_ECUDA;
     std::lock_guard<std::mutex> lk(mu);
     if (cached[dev] == 0) {
-        using Cfg = typename CfgFor<K, V>::type;
-        using Smem = SmemFor<K, V>;
+        using Smem = SmemOf<Cfg, K, V>;
         auto* kern = tile_merge_kernel<Cfg, K, V, DESC>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::total) !=
             cudaSuccess)
@@ -41,7 +40,7 @@ static om_status prepare_typed(int* resident) {
 template <typename K, bool DESC>
 static om_status typed_merge(const void* A, int64_t m, const void* B, int64_t n, void* C, cudaStream_t st) {
     int resident = 0;
-    const om_status s = prepare_typed<K, false, DESC>(&resident);
+    const om_status s = prepare_typed<typename CfgFor<K, false>::type, K, false, DESC>(&resident);
     if (s != OM_OK) return s;
     return merge_impl<K, false, DESC>(static_cast<const K*>(A), nullptr, m, static_cast<const K*>(B), nullptr, n,
                                       static_cast<K*>(C), nullptr, resident, st);
@@ -57,7 +56,7 @@ static om_status typed_merge_order(int order, const void* A, int64_t m, const vo
 template <typename K, bool V, bool DESC>
 static om_status typed_sort(void* keys, uint32_t* vals, int64_t n, cudaStream_t st) {
     int resident = 0;
-    const om_status s = prepare_typed<K, V, DESC>(&resident);
+    const om_status s = prepare_typed<typename SortCfgFor<K, V>::type, K, V, DESC>(&resident);
     if (s != OM_OK) return s;
     return sort_impl<K, V, DESC>(static_cast<K*>(keys), vals, n, resident, st);
 }

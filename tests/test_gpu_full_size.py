@@ -76,3 +76,44 @@ def test_merge_sort_full(gpu):
     wk, wv = oracle.merge_sort_pairs_u32(sub, np.arange(sub.size, dtype=np.uint32))
     assert np.array_equal(host(dk).view(np.uint32), wk)
     assert np.array_equal(host(dv).view(np.uint32), wv)
+
+
+@pytest.mark.parametrize("workload", ["f64", "i64_desc"])
+def test_merge_keys_full(gpu, workload):
+    """2^28 outputs of 8-byte keys (the benchmark's typed merges), compared
+    with the oracle over the whole output, bit for bit."""
+    d = synth.make_device(workload, "cuda")
+    desc = synth.TYPED[workload][1]
+    C = gpu.merge_keys(d["A"], d["B"], descending=desc)
+    torch.cuda.synchronize()
+    assert gpu.device_error() == 0
+    hA, hB, hC = host(d["A"]), host(d["B"]), host(C)
+    del C, d
+    torch.cuda.empty_cache()
+    want = oracle.merge_keys(hA, hB, descending=desc)
+    assert np.array_equal(hC.view(np.uint64), want.view(np.uint64)), (
+        f"first mismatch at {int(np.flatnonzero(hC.view(np.uint64) != want.view(np.uint64))[0])}")
+
+
+@pytest.mark.parametrize("workload", ["sort_f32_desc", "sort_f64"])
+def test_merge_sort_keys_full(gpu, workload):
+    """2^26 float keys through the benchmark's typed sorts: ordered, a
+    permutation of the input, and (with the index payload) stable."""
+    d = synth.make_device(workload, "cuda")
+    desc = synth.TYPED[workload][1]
+    keys0 = host(d["keys"]).copy()
+    vals = d.get("vals")
+    gpu.merge_sort_keys(d["keys"], vals, descending=desc)
+    torch.cuda.synchronize()
+    assert gpu.device_error() == 0
+    k = host(d["keys"])
+    order = k[:-1] >= k[1:] if desc else k[:-1] <= k[1:]
+    assert np.all(order), "keys out of order"
+    if vals is None:
+        assert np.array_equal(np.sort(k), np.sort(keys0)), "keys not a permutation of the input"
+    else:
+        v = host(vals).view(np.uint32)
+        assert np.array_equal(np.sort(v), np.arange(k.size, dtype=np.uint32)), "values not a permutation"
+        assert np.array_equal(keys0[v].view(np.uint32), k.view(np.uint32)), "a value does not travel with its key"
+        same = k[1:] == k[:-1]
+        assert np.all(v[1:][same] > v[:-1][same]), "equal keys out of input order (unstable)"

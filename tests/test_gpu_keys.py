@@ -94,8 +94,9 @@ def sorted_keys(rng, name, size, span, desc):
 
 @pytest.mark.parametrize("desc", [False, True], ids=["asc", "desc"])
 @pytest.mark.parametrize("name", TYPES)
-@pytest.mark.parametrize("m,n", [(0, 0), (0, 7), (7, 0), (1, 1), (1407, 1), (1408, 1408), (2944, 1),
-                                 (12345, 54321), (250001, 249999)])
+@pytest.mark.parametrize("m,n", [(0, 0), (0, 7), (7, 0), (1, 1), (1343, 1), (1344, 1344), (1407, 1), (1408, 1408),
+                                 (1471, 1), (1472, 1472), (2944, 1), (4037, 2945), (12345, 54321),
+                                 (250001, 249999)])
 def test_shapes(gpu, name, desc, m, n):
     rng = np.random.default_rng(m * 31 + n + 7 * TYPES.index(name) + desc)
     for span in (8, 1 << 30):
