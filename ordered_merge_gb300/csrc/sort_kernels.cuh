@@ -97,25 +97,83 @@ __device__ __forceinline__ int corank_padded(int d, const K* s, int a0, int m, i
     return lo;
 }
 
-template <typename Cfg, typename K, bool V, bool DESC = false>
-__global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_CTAS) block_sort_kernel(const K* in_k, const uint32_t* in_v, K* out_k,
-                                                             uint32_t* out_v, int64_t n, int run_from, int run_to) {
+// One merge step of the block sort: thread outputs [p0, p0 + VT) of the merge
+// of the two runs of length w its slice falls in, into k / v (registers);
+// returns how many of them exist (VT unless the tile is short).  FULL: the
+// tile holds TILE elements, so both runs are whole and every thread has VT
+// outputs (no length clamps or per-output guards).
+template <int VT, typename K, bool V, bool DESC, bool FULL>
+__device__ __forceinline__ int block_merge_step(const K* sk, const uint32_t* sv, int p0, int count, int w, K (&k)[VT],
+                                                uint32_t (&v)[VT]) {
+    if (!FULL && p0 >= count) return 0;
+    const int a0 = p0 & ~(2 * w - 1);
+    const int d = p0 - a0;
+    const int m = FULL ? w : ((count - a0) < w ? (count - a0) : w);
+    const int nb_raw = count - a0 - w;
+    const int nb = FULL ? w : (nb_raw <= 0 ? 0 : (nb_raw < w ? nb_raw : w));
+    const int b0 = a0 + w;
+    const int cnt = FULL ? VT : ((m + nb - d) < VT ? (m + nb - d) : VT);
+    const int a = corank_padded<K, DESC>(d, sk, a0, m, b0, nb, w);
+    // Serial merge with selects: A and B are adjacent runs, so one index
+    // reaches either head (at most one past the tile's last element: the
+    // spare slot).  Take A unless A is exhausted or B's head comes strictly
+    // before it.
+    int ia = a0 + a, ib = b0 + (d - a);
+    const int ea = a0 + m, eb = b0 + nb;
+    K ak = sk[padk<K>(ia)], bk = sk[padk<K>(ib)];
+    auto ao = OrderKey<K>::of(ak);
+    auto bo = OrderKey<K>::of(bk);
+    uint32_t av = V ? sv[pad32(ia)] : 0u, bv = V ? sv[pad32(ib)] : 0u;
+#pragma unroll
+    for (int i = 0; i < VT; ++i) {
+        if (FULL || i < cnt) {
+            const bool p = (ib >= eb) || (ia < ea && ord_first<DESC>(ao, bo));
+            k[i] = p ? ak : bk;
+            if (V) v[i] = p ? av : bv;
+            ia += p ? 1 : 0;
+            ib += p ? 0 : 1;
+            if (i + 1 < VT) {
+                const int idx = p ? ia : ib;  // at most TILE: the spare slot
+                const K nk = sk[padk<K>(idx)];
+                const auto no = OrderKey<K>::of(nk);
+                ak = p ? nk : ak;
+                bk = p ? bk : nk;
+                ao = p ? no : ao;
+                bo = p ? bo : no;
+                if (V) {
+                    const uint32_t nv = sv[pad32(idx)];
+                    av = p ? nv : av;
+                    bv = p ? bv : nv;
+                }
+            }
+        }
+    }
+    return cnt;
+}
+
+// The work of one CTA on its tile of `count` elements.  FULL (count ==
+// TILE, every tile but the last): the loops over the tile are unrolled and
+// carry no bounds tests.
+template <typename Cfg, typename K, bool V, bool DESC, bool FULL>
+__device__ __forceinline__ void block_sort_tile(const K* in_k, const uint32_t* in_v, K* out_k, uint32_t* out_v,
+                                                int64_t base, int count, int run_from, int run_to, K* sk,
+                                                uint32_t* sv) {
     constexpr int NT = Cfg::NT;
     constexpr int VT = Cfg::VT;
-    constexpr int TILE = Cfg::TILE;
-    constexpr int PADDED_K = block_sort_key_slots<Cfg, K>();
-    static_assert(!V || sizeof(K) == 4, "values ride with 4-byte keys");
-    extern __shared__ __align__(16) unsigned char bsm_raw[];
-    K* sk = reinterpret_cast<K*>(bsm_raw);
-    uint32_t* sv = V ? reinterpret_cast<uint32_t*>(sk + PADDED_K) : nullptr;
-
     const int tid = threadIdx.x;
-    const int64_t base = (int64_t)blockIdx.x * TILE;
-    const int count = (int)((n - base) < TILE ? (n - base) : TILE);
 
-    for (int p = tid; p < count; p += NT) {
-        sk[padk<K>(p)] = in_k[base + p];
-        if (V) sv[pad32(p)] = in_v[base + p];
+    if (FULL) {
+#pragma unroll
+        for (int j = 0; j < VT; ++j) {
+            const int p = tid + j * NT;
+            sk[padk<K>(p)] = in_k[base + p];
+            if (V) sv[pad32(p)] = in_v[base + p];
+        }
+    } else {
+        for (int p = tid; p < count; p += NT) {
+            sk[padk<K>(p)] = in_k[base + p];
+            if (V) sv[pad32(p)] = in_v[base + p];
+        }
     }
     __syncthreads();
 
@@ -129,7 +187,7 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_CTAS) block_sort_kernel(cons
         // needs the left key strictly after the right one in the order).
 #pragma unroll
         for (int i = 0; i < VT; ++i) {
-            const bool real = p0 + i < count;
+            const bool real = FULL || p0 + i < count;
             k[i] = real ? sk[padk<K>(p0 + i)] : last_key<K, DESC>();
             if (V) v[i] = real ? sv[pad32(p0 + i)] : 0u;
         }
@@ -152,7 +210,7 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_CTAS) block_sort_kernel(cons
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < VT; ++i) {
-            if (p0 + i < count) {
+            if (FULL || p0 + i < count) {
                 sk[padk<K>(p0 + i)] = k[i];
                 if (V) sv[pad32(p0 + i)] = v[i];
             }
@@ -162,57 +220,11 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_CTAS) block_sort_kernel(cons
     }
 
     for (; w < run_to; w *= 2) {
-        int cnt = 0;
-        if (p0 < count) {
-            const int a0 = p0 & ~(2 * w - 1);
-            const int d = p0 - a0;
-            const int m = (count - a0) < w ? (count - a0) : w;
-            const int nb_raw = count - a0 - w;
-            const int nb = nb_raw <= 0 ? 0 : (nb_raw < w ? nb_raw : w);
-            const int b0 = a0 + w;
-            cnt = (m + nb - d) < VT ? (m + nb - d) : VT;
-            const int a = corank_padded<K, DESC>(d, sk, a0, m, b0, nb, w);
-            // Serial merge with selects: A and B are adjacent runs, so one
-            // index reaches either head (at most one past the tile's last
-            // element: the spare slot).  Take A unless A is exhausted or B's
-            // head comes strictly before it.
-            int ia = a0 + a, ib = b0 + (d - a);
-            const int ea = a0 + m, eb = b0 + nb;
-            const int x = ia;  // at most TILE: the spare slot
-            const int y = ib;
-            K ak = sk[padk<K>(x)], bk = sk[padk<K>(y)];
-            auto ao = OrderKey<K>::of(ak);
-            auto bo = OrderKey<K>::of(bk);
-            uint32_t av = V ? sv[pad32(x)] : 0u, bv = V ? sv[pad32(y)] : 0u;
-#pragma unroll
-            for (int i = 0; i < VT; ++i) {
-                if (i < cnt) {
-                    const bool p = (ib >= eb) || (ia < ea && ord_first<DESC>(ao, bo));
-                    k[i] = p ? ak : bk;
-                    if (V) v[i] = p ? av : bv;
-                    ia += p ? 1 : 0;
-                    ib += p ? 0 : 1;
-                    if (i + 1 < VT) {
-                        const int idx = p ? ia : ib;  // at most TILE: the spare slot
-                        const K nk = sk[padk<K>(idx)];
-                        const auto no = OrderKey<K>::of(nk);
-                        ak = p ? nk : ak;
-                        bk = p ? bk : nk;
-                        ao = p ? no : ao;
-                        bo = p ? bo : no;
-                        if (V) {
-                            const uint32_t nv = sv[pad32(idx)];
-                            av = p ? nv : av;
-                            bv = p ? bv : nv;
-                        }
-                    }
-                }
-            }
-        }
+        const int cnt = block_merge_step<VT, K, V, DESC, FULL>(sk, sv, p0, count, w, k, v);
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < VT; ++i) {
-            if (i < cnt) {
+            if (FULL || i < cnt) {
                 sk[padk<K>(p0 + i)] = k[i];
                 if (V) sv[pad32(p0 + i)] = v[i];
             }
@@ -220,9 +232,37 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_CTAS) block_sort_kernel(cons
         __syncthreads();
     }
 
-    for (int p = tid; p < count; p += NT) {
-        out_k[base + p] = sk[padk<K>(p)];
-        if (V) out_v[base + p] = sv[pad32(p)];
+    if (FULL) {
+#pragma unroll
+        for (int j = 0; j < VT; ++j) {
+            const int p = tid + j * NT;
+            out_k[base + p] = sk[padk<K>(p)];
+            if (V) out_v[base + p] = sv[pad32(p)];
+        }
+    } else {
+        for (int p = tid; p < count; p += NT) {
+            out_k[base + p] = sk[padk<K>(p)];
+            if (V) out_v[base + p] = sv[pad32(p)];
+        }
+    }
+}
+
+template <typename Cfg, typename K, bool V, bool DESC = false>
+__global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_CTAS) block_sort_kernel(const K* in_k, const uint32_t* in_v, K* out_k,
+                                                             uint32_t* out_v, int64_t n, int run_from, int run_to) {
+    constexpr int TILE = Cfg::TILE;
+    constexpr int PADDED_K = block_sort_key_slots<Cfg, K>();
+    static_assert(!V || sizeof(K) == 4, "values ride with 4-byte keys");
+    extern __shared__ __align__(16) unsigned char bsm_raw[];
+    K* sk = reinterpret_cast<K*>(bsm_raw);
+    uint32_t* sv = V ? reinterpret_cast<uint32_t*>(sk + PADDED_K) : nullptr;
+
+    const int64_t base = (int64_t)blockIdx.x * TILE;
+    const int count = (int)((n - base) < TILE ? (n - base) : TILE);
+    if (count == TILE) {
+        block_sort_tile<Cfg, K, V, DESC, true>(in_k, in_v, out_k, out_v, base, TILE, run_from, run_to, sk, sv);
+    } else {
+        block_sort_tile<Cfg, K, V, DESC, false>(in_k, in_v, out_k, out_v, base, count, run_from, run_to, sk, sv);
     }
 }
 
