@@ -74,10 +74,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, units_per_launch: int):
     """Per-launch DRAM bytes (read + write) of the tile-merge kernel on this
-    workload from the committed ncu summary, or None when there is none or
-    the kernel sources changed since it was taken."""
+    workload from the committed ncu summary, or None when there is none, the
+    kernel sources changed since it was taken, or it was taken at another
+    size (a scaled run)."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -86,7 +87,9 @@ def recorded_traffic(workload: str):
     if rec.get("source_hash") != kernel_source_hash():
         return None
     wl = rec.get("workloads", {}).get(workload)
-    return wl.get("traffic_bytes_per_launch") if wl else None
+    if not wl or wl.get("units_per_launch") != units_per_launch:
+        return None
+    return wl.get("traffic_bytes_per_launch")
 
 
 def load_peak():
@@ -419,7 +422,7 @@ def bench_ours(args):
     alg_bytes = total * bytes_per_elem
     tm_avg_ms = tm_ms / tm_launches if tm_launches else float("nan")
     achieved = alg_bytes / (tm_avg_ms / 1e3) / 1e9 if tm_launches else None
-    traffic = recorded_traffic(wl)
+    traffic = recorded_traffic(wl, total)
     roofline = {
         "kernel": "tile_merge_kernel",
         "bound": "hbm",

@@ -83,3 +83,23 @@ def test_clock_summary(tmp_path):
     assert out["sm_max_mhz"] == 2070 and out["samples"] == 3
     assert out["sm_mhz"] == pytest.approx(1985.0)
     assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_recorded_traffic_matches_sources_and_size(tmp_path, monkeypatch):
+    """The committed DRAM traffic is reported only for the kernel sources and
+    the launch size it was taken on."""
+    import json
+
+    import bench
+
+    rec = {"source_hash": bench.kernel_source_hash(),
+           "workloads": {"uniform": {"units_per_launch": 1 << 29, "traffic_bytes_per_launch": 4_000_000_000}}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
+    assert bench.recorded_traffic("uniform", 1 << 29) == 4_000_000_000
+    assert bench.recorded_traffic("uniform", 1 << 26) is None  # a scaled run
+    assert bench.recorded_traffic("skewed", 1 << 29) is None  # no record
+    rec["source_hash"] = "0" * 16
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("uniform", 1 << 29) is None  # kernels changed since
