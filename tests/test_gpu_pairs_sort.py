@@ -123,6 +123,30 @@ def test_sort_workload_scaled(gpu):
     check_sort(gpu, d["keys"])
 
 
+@pytest.mark.parametrize("per_range", [1, 3])
+@pytest.mark.parametrize("n", [200001, (1 << 18) + 4097])
+def test_sort_pairs_split_into_ranges(gpu, monkeypatch, per_range, n):
+    """Late passes whose pairs of runs split into several output ranges (as
+    at full size), with a ragged last pair: short ranges forced."""
+    monkeypatch.setenv("OM_SUBTILES_PER_RANGE", str(per_range))
+    rng = np.random.default_rng(per_range * 7 + n)
+    check_sort(gpu, rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32))
+    check_sort(gpu, rng.integers(0, 50, n, dtype=np.uint64).astype(np.uint32))
+
+
+@pytest.mark.parametrize("waves", [2, 5])
+def test_merge_and_sort_forced_waves(gpu, monkeypatch, waves):
+    """The range rule held to a fixed wave count: several waves of shorter
+    ranges give the same merge and sort."""
+    monkeypatch.setenv("OM_WAVES", str(waves))
+    rng = np.random.default_rng(waves)
+    ka = np.sort(rng.integers(0, 1000, 300007, dtype=np.uint64).astype(np.uint32))
+    kb = np.sort(rng.integers(0, 1000, 200003, dtype=np.uint64).astype(np.uint32))
+    va, vb = tagged(ka.size, kb.size)
+    check_pairs(gpu, ka, va, kb, vb)
+    check_sort(gpu, rng.integers(0, 1 << 32, 300007, dtype=np.uint64).astype(np.uint32))
+
+
 @pytest.mark.parametrize("per_range", [8, 40])
 def test_pairs_long_ranges_uneven_consumption(gpu, monkeypatch, per_range):
     """Key+value merge with many sub-tiles per range and bursty consumption."""
