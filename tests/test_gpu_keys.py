@@ -269,3 +269,47 @@ def test_sort_u32_typed_matches_merge_sort_u32(gpu):
     gpu.merge_sort_keys(k2, v2, key_type="u32")
     torch.cuda.synchronize()
     assert torch.equal(k1, k2) and torch.equal(v1, v2)
+
+
+@pytest.mark.parametrize("name", ["f32", "f64", "i64"])
+def test_unsorted_or_nan_input_terminates_in_bounds(gpu, name):
+    """NaN keys (no place in the order) and unsorted keys break the merge's
+    precondition: the output is unspecified, but every kernel ends, writes
+    nothing outside its output, and the error word reports at most a dropped
+    range, never a timed-out wait.  The same holds for the in-place sort of
+    keys holding NaN (a NaN makes the order intransitive, so neighbouring
+    co-rank searches may disagree and the result need not be a permutation);
+    without NaN the sort of the same unsorted keys is checked exactly."""
+    npc, tc = _carrier(name)
+    dt = NP[name]
+    rng = np.random.default_rng(TYPES.index(name))
+    for m, n in [(70001, 50003), (5000, 3)]:
+        A = rng.integers(-1000, 1000, m).astype(dt)
+        B = rng.integers(-1000, 1000, n).astype(dt)
+        if np.issubdtype(dt, np.floating):
+            A[rng.integers(0, m, m // 10)] = np.nan
+            B = np.sort(B)
+            B[n // 2] = np.nan
+        total = m + n
+        sentinel = -0x5A5A5A5B
+        buf = torch.full((total + 2 * GUARD + 4,), sentinel, dtype=tc, device="cuda")
+        C = buf[GUARD: GUARD + total]
+        for desc in (False, True):
+            gpu.merge_keys(to_dev(A, name), to_dev(B, name), C, key_type=name, descending=desc)
+            torch.cuda.synchronize()
+            assert gpu.device_error() in (0, 2), "a kernel wait timed out"
+            h = buf.cpu().numpy()
+            assert np.all(h[:GUARD] == sentinel) and np.all(h[GUARD + total:] == sentinel), "merge wrote outside C"
+        # in-place sort of the same keys inside guard bands
+        keys = np.concatenate([A, B])
+        sbuf = torch.full((total + 2 * GUARD + 4,), sentinel, dtype=tc, device="cuda")
+        K = sbuf[GUARD: GUARD + total]
+        K.copy_(torch.from_numpy(keys.view(npc)))
+        gpu.merge_sort_keys(K, key_type=name)
+        torch.cuda.synchronize()
+        assert gpu.device_error() in (0, 2), "a sort wait timed out"
+        h = sbuf.cpu().numpy()
+        assert np.all(h[:GUARD] == sentinel) and np.all(h[GUARD + total:] == sentinel), "sort wrote outside its keys"
+        if not np.issubdtype(dt, np.floating):
+            # no NaN: an ordinary sort of unsorted keys, fully defined
+            assert np.array_equal(K.cpu().numpy().view(dt), np.sort(keys)), "int64 sort differs"
