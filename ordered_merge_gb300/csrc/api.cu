@@ -87,6 +87,12 @@ static std::vector<cudaEvent_t> g_event_pool;
 static int64_t g_trace_launches[kNumKinds];
 static double g_trace_ms[kNumKinds];
 
+static void trace_collect_locked();
+
+// Launches traced but not yet read are summed (waiting for their events)
+// once this many are pending, so tracing left on keeps bounded state.
+static constexpr size_t kMaxPendingTraces = 1 << 16;
+
 static cudaEvent_t pool_event() {
     if (!g_event_pool.empty()) {
         cudaEvent_t e = g_event_pool.back();
@@ -107,6 +113,12 @@ bool trace_begin(int kind, cudaStream_t stream, TraceRec* rec) {
         if (on) {
             rec->e0 = pool_event();
             rec->e1 = pool_event();
+            if (rec->e0 == nullptr || rec->e1 == nullptr) {  // no events to be had: this launch goes untraced
+                if (rec->e0) g_event_pool.push_back(rec->e0);
+                if (rec->e1) g_event_pool.push_back(rec->e1);
+                cudaGetLastError();
+                on = false;
+            }
         }
     }
     if (on) cudaEventRecord(rec->e0, stream);
@@ -120,6 +132,7 @@ cudaError_t trace_end(const TraceRec& rec, bool on, cudaStream_t stream) {
         cudaEventRecord(rec.e1, stream);
         std::lock_guard<std::mutex> lk(g_trace_mu);
         g_trace_recs.push_back(rec);
+        if (g_trace_recs.size() >= kMaxPendingTraces) trace_collect_locked();
     }
     return e;
 }
