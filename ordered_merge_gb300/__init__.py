@@ -106,10 +106,20 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _ptr4(t, name: str):
-    """Device pointer of a contiguous CUDA tensor of 4-byte elements."""
+def _on_current_device(t, name: str):
+    """The library launches on the current CUDA device: a tensor elsewhere
+    would hand that device's addresses to its kernels."""
+    import torch
+
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
+
+
+def _ptr4(t, name: str):
+    """Device pointer of a contiguous CUDA tensor of 4-byte elements."""
+    _on_current_device(t, name)
     if t.element_size() != 4:
         raise ValueError(f"{name} must have 4-byte elements (got {t.dtype})")
     if not t.is_contiguous():
@@ -131,8 +141,12 @@ def om_corank_i32_batch(ks, A, B, out=None, stream=None):
 
     if ks.dtype != torch.int64 or not ks.is_cuda or not ks.is_contiguous():
         raise ValueError("ks must be a contiguous int64 CUDA tensor")
+    _on_current_device(ks, "ks")
     if out is None:
         out = torch.empty_like(ks)
+    if out.dtype != torch.int64 or out.numel() != ks.numel() or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int64 tensor as long as ks")
+    _on_current_device(out, "out")
     _check(
         _lib.om_corank_i32_batch(ks.data_ptr() if ks.numel() else None, ks.numel(), _ptr4(A, "A"), A.numel(),
                                  _ptr4(B, "B"), B.numel(), out.data_ptr() if out.numel() else None,
@@ -171,8 +185,7 @@ def _key_type_of(dtype) -> str:
 
 def _ptr_sized(t, name: str, size: int):
     """Device pointer of a contiguous CUDA tensor of `size`-byte elements."""
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    _on_current_device(t, name)
     if t.element_size() != size:
         raise ValueError(f"{name} must have {size}-byte elements (got {t.dtype})")
     if not t.is_contiguous():
