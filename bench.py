@@ -734,7 +734,7 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--workload", default="uniform", choices=sorted(WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--e2e-steps", type=int, default=8)
+    p.add_argument("--e2e-steps", type=int, default=32)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ref-budget-s", type=float, default=60.0,
                    help="reference arm: CPU seconds the K + W oracle steps should take in total")
