@@ -313,3 +313,29 @@ def test_unsorted_or_nan_input_terminates_in_bounds(gpu, name):
         if not np.issubdtype(dt, np.floating):
             # no NaN: an ordinary sort of unsorted keys, fully defined
             assert np.array_equal(K.cpu().numpy().view(dt), np.sort(keys)), "int64 sort differs"
+
+
+@pytest.mark.parametrize("name", TYPES)
+@pytest.mark.parametrize("offs", [(0, 0, 0), (1, 0, 0), (0, 1, 3), (3, 2, 1), (2, 3, 0), (1, 1, 1)])
+def test_one_sided_ranges(gpu, name, offs):
+    """Output ranges that take every element from one side: A wholly before
+    B (and B wholly before A), runs that alternate in long blocks, every
+    16-byte phase of A, B and C, both orders."""
+    if np.dtype(NP[name]).itemsize == 8:
+        offs = tuple(o & 1 for o in offs)
+    rng = np.random.default_rng(sum(offs) * 7 + TYPES.index(name))
+    for desc in (False, True):
+        lo = np.sort(rng.integers(0, 1 << 20, 300001)).astype(NP[name])
+        hi = np.sort(rng.integers(1 << 20, 1 << 21, 200003)).astype(NP[name])
+        A, B = (lo, hi) if not desc else (hi[::-1].copy(), lo[::-1].copy())
+        check(gpu, name, A, B, desc, offs)
+        check(gpu, name, B, A, desc, offs)
+        # long alternating blocks: most ranges one-sided, a few straddle a block edge
+        blocks = np.arange(2 * 40 * 9000).reshape(80, 9000)
+        keys = (blocks // 3).astype(NP[name]) if not np.issubdtype(NP[name], np.floating) \
+            else (blocks / 3.0).astype(NP[name])
+        A2 = np.sort(keys[0::2].ravel())
+        B2 = np.sort(keys[1::2].ravel())
+        if desc:
+            A2, B2 = A2[::-1].copy(), B2[::-1].copy()
+        check(gpu, name, A2, B2, desc, offs)

@@ -69,6 +69,22 @@ def test_pairs_misaligned(gpu, offs):
     check_pairs(gpu, ka, va, kb, vb, offs)
 
 
+@pytest.mark.parametrize("offs", [(0, 0, 0), (1, 0, 0), (0, 2, 3), (3, 1, 2), (2, 2, 1)])
+def test_pairs_one_sided_ranges(gpu, offs):
+    """Key+value output ranges that take every element from one side, at
+    every 16-byte phase of A, B and C."""
+    rng = np.random.default_rng(sum(offs) + 17)
+    lo = np.sort(rng.integers(0, 1 << 20, 250007)).astype(np.uint32)
+    hi = np.sort(rng.integers(1 << 20, 1 << 21, 180001)).astype(np.uint32)
+    for ka, kb in ((lo, hi), (hi, lo)):
+        va, vb = tagged(ka.size, kb.size)
+        check_pairs(gpu, ka, va, kb, vb, offs)
+    blocks = (np.arange(60 * 7000).reshape(60, 7000) // 5).astype(np.uint32)
+    ka, kb = np.sort(blocks[0::2].ravel()), np.sort(blocks[1::2].ravel())
+    va, vb = tagged(ka.size, kb.size)
+    check_pairs(gpu, ka, va, kb, vb, offs)
+
+
 def test_pairs_ties_workload_scaled(gpu):
     d = synth.make_host("pairs_ties", scale_log2=4)
     check_pairs(gpu, d["keysA"], d["valsA"], d["keysB"], d["valsB"])
