@@ -507,21 +507,27 @@ def bench_ours(args):
         for i in range(nbuf):
             e2e_step(i)
         torch.cuda.synchronize(device)
-        barrier(world, device)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for st in streams:
-            st.wait_event(e0)
-        for i in range(args.e2e_steps):
-            e2e_step(i)
-        for st in streams:
-            stream.wait_stream(st)
-        e1.record(stream)
-        torch.cuda.synchronize(device)
-        e_ms = reduce_max(e0.elapsed_time(e1), world, device)
-        if not torch.equal(hC[(args.e2e_steps - 1) % nbuf].to(device), C if nbuf == 1 else dC[0]):
-            raise RuntimeError("end-to-end result differs from the device-resident merge")
+        # Three timed runs of e2e_steps pipelined calls; the median run is
+        # reported (the host link and host memory are shared with the
+        # machine's other jobs, so single runs vary).
+        run_ms = []
+        for _ in range(3):
+            barrier(world, device)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for st in streams:
+                st.wait_event(e0)
+            for i in range(args.e2e_steps):
+                e2e_step(i)
+            for st in streams:
+                stream.wait_stream(st)
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            run_ms.append(reduce_max(e0.elapsed_time(e1), world, device))
+            if not torch.equal(hC[(args.e2e_steps - 1) % nbuf].to(device), C if nbuf == 1 else dC[0]):
+                raise RuntimeError("end-to-end result differs from the device-resident merge")
+        e_ms = sorted(run_ms)[1]
         e2e = {
             "value": world * total * args.e2e_steps / (e_ms / 1e3),
             "unit": UNIT,
@@ -529,6 +535,8 @@ def bench_ours(args):
             "d2h_bytes_per_step": total * 4,
             "steps": args.e2e_steps,
             "ms_per_step": e_ms / args.e2e_steps,
+            "ms_per_step_runs": [round(x / args.e2e_steps, 3) for x in run_ms],
+            "timing": "median of 3 timed runs of `steps` pipelined calls",
             "streams": "3 (copy in, merge, copy out), 2 buffer sets",
             "h2d_gbs_single_copy": round(h2d_gbs, 1),
             "d2h_gbs_single_copy": round(d2h_gbs, 1),
@@ -734,7 +742,7 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--workload", default="uniform", choices=sorted(WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--e2e-steps", type=int, default=32)
+    p.add_argument("--e2e-steps", type=int, default=16)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ref-budget-s", type=float, default=60.0,
                    help="reference arm: CPU seconds the K + W oracle steps should take in total")
