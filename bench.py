@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "merged elements/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "elements/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 WORKLOADS = {
     "uniform": "int32 merge at bandwidth scale: A, B = 2^28 sorted uniform full-range int32 each",
@@ -596,6 +597,8 @@ def bench_ours(args):
         }
         if line["achieved_gbs"] is not None:
             line["pct_of_hbm_peak"] = round(100.0 * line["achieved_gbs"] / peak, 2)
+            # the same against the nominal HBM3e bandwidth of one GB300 (context)
+            line["pct_of_nominal_hbm"] = round(100.0 * line["achieved_gbs"] / NOMINAL_HBM_GBS, 2)
         print(json.dumps(line), flush=True)
     barrier(world, device)
 
