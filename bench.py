@@ -5,8 +5,9 @@
 
 Default workload: int32 merge of two sorted uniform full-range arrays,
 m = n = 2^28 (2^29 outputs, 2 GiB read + 2 GiB written per merge).  One step
-= one om_merge_i32 call (partition kernel + tile-merge kernel) on inputs
-already resident in HBM.  Prints ONE JSON line on rank 0.
+= one om_merge_i32 call (one tile-merge launch whose CTAs find their own
+range boundaries) on inputs already resident in HBM.  Prints ONE JSON line on
+rank 0.
 
   value      merged elements/s over the K timed steps (CUDA events on the
              launching stream; max over ranks for N > 1, times N replicas)
@@ -17,6 +18,8 @@ already resident in HBM.  Prints ONE JSON line on rank 0.
              region: pinned host A, B -> device, merge, device C -> pinned host
   cpu_baseline  the CPU oracle (single thread) on the same workload
   clocks     nvidia-smi samples taken during the timed region
+  other_configs  the evens/odds, heavy-tie pairs, skewed and sort workloads,
+             each timed the same way in the same run with fewer steps
 
 --impl reference times the CPU oracle alone on a bounded sample per step.
 N > 1 runs independent replicas (the merge needs no exchange across GPUs in
@@ -279,21 +282,20 @@ def oracle_rate(wl: str, h: dict, budget_s: float = 12.0, max_reps: int = 5):
 
 # ------------------------------------------------------------- our arm --
 
-def bench_ours(args):
-    import numpy as np
+def measure(wl: str, args, device, world: int, steps: int, warmup: int, keep: bool = False):
+    """Times `steps` calls of workload `wl` after `warmup` untimed ones (CUDA
+    events on the launching stream; L2 flushed before every timed call when
+    the bytes a call moves fit twice in L2) and returns the figures of one
+    bench line: time, rate, the tile-merge kernel's roofline and the clocks
+    sampled meanwhile.  keep: also return the device tensors (end-to-end leg)."""
     import torch
 
     import ordered_merge_gb300 as om
     import synth
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist_init(world, "nccl")
-
-    wl = args.workload
     d = synth.make_device(wl, device, scale_log2=args.scale_log2)
     stream = torch.cuda.current_stream(device)
+    tensors = {}
 
     if wl in ("uniform", "evens_odds", "skewed"):
         A, B = d["A"], d["B"]
@@ -302,7 +304,7 @@ def bench_ours(args):
         bytes_per_elem = 8
         C = torch.empty(total, dtype=torch.int32, device=device)
         step = lambda: om.merge_i32(A, B, C)
-        units_per_step = total
+        tensors = {"A": A, "B": B, "C": C}
     elif wl in ("f64", "i64_desc"):
         kt, desc = synth.TYPED[wl]
         A, B = d["A"], d["B"]
@@ -311,7 +313,6 @@ def bench_ours(args):
         bytes_per_elem = 2 * A.element_size()
         C = torch.empty(total, dtype=A.dtype, device=device)
         step = lambda: om.merge_keys(A, B, C, key_type=kt, descending=desc)
-        units_per_step = total
     elif wl == "pairs_ties":
         ka, va, kb, vb = d["keysA"], d["valsA"], d["keysB"], d["valsB"]
         m, n = ka.numel(), kb.numel()
@@ -320,7 +321,6 @@ def bench_ours(args):
         kc = torch.empty(total, dtype=torch.int32, device=device)
         vc = torch.empty_like(kc)
         step = lambda: om.merge_pairs_u32(ka, va, kb, vb, kc, vc)
-        units_per_step = total
     else:  # sorts: restore the unsorted input before each step (outside the timed events)
         keys0, vals0 = d["keys"], d.get("vals")
         m, n = keys0.numel(), 0
@@ -331,7 +331,6 @@ def bench_ours(args):
         vals = vals0.clone() if vals0 is not None else None
         kt, desc = synth.TYPED.get(wl, ("u32", False))
         step = None
-        units_per_step = total
 
         def sort_once():
             keys.copy_(keys0)
@@ -344,12 +343,13 @@ def bench_ours(args):
             else:
                 om.merge_sort_keys(keys, vals, key_type=kt, descending=desc)
 
+    units_per_step = total
     # ---- warm-up, then K timed steps.  A workload whose bytes moved per step
     # fit twice in L2 gets L2 flushed before every step (a write larger than
     # L2, outside the timed events); larger ones stream back to back.
     flush = L2Flusher(device) if total * bytes_per_elem < 2 * L2Flusher.l2_bytes(device) else None
     if step is not None:
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
         torch.cuda.synchronize(device)
         if om.device_error() != 0:
@@ -359,19 +359,19 @@ def bench_ours(args):
         om.om_trace_reset()
         om.om_trace_enable(True)
         launches0 = om.om_launch_count()
-        with ClockSampler(local) as clk:
+        with ClockSampler(device.index) as clk:
             if flush is None:
                 ev0 = torch.cuda.Event(enable_timing=True)
                 ev1 = torch.cuda.Event(enable_timing=True)
                 ev0.record(stream)
-                for _ in range(args.steps):
+                for _ in range(steps):
                     step()
                 ev1.record(stream)
                 torch.cuda.synchronize(device)
                 ms = ev0.elapsed_time(ev1)
             else:
                 pairs = []
-                for _ in range(args.steps):
+                for _ in range(steps):
                     flush()
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
@@ -384,7 +384,7 @@ def bench_ours(args):
         launches = om.om_launch_count() - launches0
         om.om_trace_enable(False)
     else:
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             sort_once()
             sort_call()
         torch.cuda.synchronize(device)
@@ -393,8 +393,8 @@ def bench_ours(args):
         om.om_trace_enable(True)
         launches0 = om.om_launch_count()
         ms = 0.0
-        with ClockSampler(local) as clk:
-            for _ in range(args.steps):
+        with ClockSampler(device.index) as clk:
+            for _ in range(steps):
                 sort_once()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
@@ -410,11 +410,7 @@ def bench_ours(args):
     clocks = clk.summary()
 
     ms_max = reduce_max(ms, world, device)
-    ms_per_step = ms_max / args.steps
-    value = world * units_per_step * args.steps / (ms_max / 1e3)
-
     tm_launches, tm_ms = om.om_trace_read(om.KIND_TILE_MERGE)
-    p_launches, p_ms = om.om_trace_read(om.KIND_PARTITION)
     bs_launches, bs_ms = om.om_trace_read(om.KIND_BLOCK_SORT)
     peak, peak_src = load_peak()
     # merges: one launch moves every element once (read + written); sorts: the
@@ -423,7 +419,6 @@ def bench_ours(args):
     alg_bytes = total * bytes_per_elem
     tm_avg_ms = tm_ms / tm_launches if tm_launches else float("nan")
     achieved = alg_bytes / (tm_avg_ms / 1e3) / 1e9 if tm_launches else None
-    traffic = recorded_traffic(wl, total)
     roofline = {
         "kernel": "tile_merge_kernel",
         "bound": "hbm",
@@ -432,16 +427,83 @@ def bench_ours(args):
         "peak_source": peak_src,
         "unit": "GB/s",
         "frac": round(achieved / peak, 4) if achieved else None,
-        "traffic": traffic,
+        "traffic": recorded_traffic(wl, total),
         "alg_bytes_per_launch": alg_bytes,
         "mean_launch_ms": round(tm_avg_ms, 5),
         "launches": tm_launches,
     }
-    kernel_share = {
-        "tile_merge_ms": round(tm_ms, 4),
-        "partition_ms": round(p_ms, 4),
-        "block_sort_ms": round(bs_ms, 4),
+    out = {
+        "wl": wl, "m": m, "n": n, "total": total, "bytes_per_elem": bytes_per_elem,
+        "steps": steps, "ms": ms, "ms_max": ms_max, "ms_per_step": ms_max / steps,
+        "value": world * units_per_step * steps / (ms_max / 1e3),
+        "achieved_gbs": (round(units_per_step * bytes_per_elem * steps / (ms / 1e3) / 1e9, 1)
+                         if wl not in SORTS else None),
+        "flushed": flush is not None, "roofline": roofline, "launches": launches, "clocks": clocks,
+        "kernel_time_ms": {"tile_merge_ms": round(tm_ms, 4), "block_sort_ms": round(bs_ms, 4),
+                           "block_sort_launches": bs_launches},
+        "peak": peak,
     }
+    if keep:
+        out["tensors"] = tensors
+    return out
+
+
+# configs measured beside the headline one in the same run, with fewer steps
+OTHER_CONFIGS = ("evens_odds", "pairs_ties", "skewed", "sort")
+
+
+def other_config_line(r: dict) -> dict:
+    """The short record of one extra config in the bench line."""
+    rec = {
+        "workload": WORKLOADS[r["wl"]],
+        "m": r["m"],
+        "n": r["n"],
+        "steps": r["steps"],
+        "ms_per_step": round(r["ms_per_step"], 5),
+        "value": r["value"],
+        "unit": UNIT,
+        "achieved_gbs": r["achieved_gbs"],
+        "tile_merge_frac_of_peak": r["roofline"]["frac"],
+        "tile_merge_mean_launch_ms": r["roofline"]["mean_launch_ms"],
+        "l2": "flushed before every timed step" if r["flushed"] else "inputs larger than L2 (no flush)",
+        "clocks": {k: r["clocks"].get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "gpu_launches": r["launches"],
+    }
+    if r["wl"] in SORTS:
+        # all passes: one block pass and the late passes, each moving every pair once
+        passes = 1 + r["roofline"]["launches"] // max(1, r["steps"])
+        rec["passes"] = passes
+        rec["pass_bytes_gbs"] = round(passes * r["total"] * r["bytes_per_elem"] / (r["ms_per_step"] / 1e3) / 1e9, 1)
+        rec["block_sort_mean_launch_ms"] = round(r["kernel_time_ms"]["block_sort_ms"]
+                                                 / max(1, r["kernel_time_ms"]["block_sort_launches"]), 5)
+    elif r["achieved_gbs"] is not None:
+        rec["pct_of_hbm_peak"] = round(100.0 * r["achieved_gbs"] / r["peak"], 2)
+    return rec
+
+
+def bench_ours(args):
+    import torch
+
+    import ordered_merge_gb300 as om
+    import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+
+    wl = args.workload
+    r = measure(wl, args, device, world, args.steps, args.warmup, keep=True)
+    m, n, total = r["m"], r["n"], r["total"]
+    ms, ms_per_step, value = r["ms"], r["ms_per_step"], r["value"]
+    roofline, kernel_share, launches, clocks, peak = (r["roofline"], r["kernel_time_ms"], r["launches"],
+                                                      r["clocks"], r["peak"])
+    flush = r["flushed"] or None
+    units_per_step, bytes_per_elem = total, r["bytes_per_elem"]
+    stream = torch.cuda.current_stream(device)
+    if wl in ("uniform", "evens_odds", "skewed"):
+        A, B, C = r["tensors"]["A"], r["tensors"]["B"], r["tensors"]["C"]
+    r.pop("tensors", None)
 
     # ---- end to end through the C-ABI call with host buffers
     # Every step copies its inputs from pinned host memory, merges and copies
@@ -544,6 +606,19 @@ def bench_ours(args):
         }
         del dA, dB, dC, hC
 
+    # ---- the other configs, measured the same way in the same process
+    others = None
+    if not args.no_other_configs and args.scale_log2 == 0:
+        A = B = C = None
+        torch.cuda.empty_cache()
+        others = {}
+        for ow in OTHER_CONFIGS:
+            if ow == wl:
+                continue
+            k = max(5, min(args.steps, 20 if ow in SORTS else 100))
+            others[ow] = other_config_line(measure(ow, args, device, world, k, args.warmup))
+            torch.cuda.empty_cache()
+
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -586,10 +661,10 @@ def bench_ours(args):
                       "L2 flushed before every timed step (a write of 2x L2, outside the timed events)",
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
-            "achieved_gbs": round(units_per_step * bytes_per_elem * args.steps
-                                  / (ms / 1e3) / 1e9, 1) if wl not in SORTS else None,
+            "achieved_gbs": r["achieved_gbs"],
             "roofline": roofline,
             "kernel_time_ms": kernel_share,
+            "other_configs": others,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches,
@@ -747,6 +822,8 @@ def main(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=16)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-other-configs", action="store_true",
+                   help="skip the other configs the line records beside the headline one")
     p.add_argument("--ref-budget-s", type=float, default=60.0,
                    help="reference arm: CPU seconds the K + W oracle steps should take in total")
     p.add_argument("--scale-log2", type=int, default=0,

@@ -33,7 +33,7 @@
  *    om_device_error().
  *  - Merges allocate nothing.  The sorts' scratch (their second key and
  *    value buffers) is taken from the library's own stream-ordered memory
- *    pool on `stream`
+ *    pool (created by the first sort on each device) on `stream`
  *    (cudaMallocFromPoolAsync) and freed on the same stream (cudaFreeAsync),
  *    so it is stream-ordered; failure returns OM_ENOMEM.  The pool keeps
  *    freed scratch mapped for later calls, so a device holds up to the
@@ -81,10 +81,27 @@ om_status om_corank_i32_batch(const int64_t *ks, int64_t count,
                               int64_t *i_out, void *stream);
 
 /*
+ * Grid-level merge-path partition: split[t] = co_rank(min(t * tile, m + n))
+ * for t < count, one co-rank search per output tile boundary, run by one
+ * warp each (32 probes per round) in a single launch on `stream`
+ * ("Tiled 與 Circular Buffer Merge Kernel (Memory Coalescing)",
+ * §Block-Level Co-Rank: one co-rank per block's output tile; "Co-rank
+ * Function 實作與 Basic Parallel Merge Kernel", §Co-rank Function 定義與不變式).
+ * The caller derives j_t = min(t * tile, m + n) - split[t].  split is a
+ * device array of count int64 owned by the caller, 8-byte aligned, not
+ * overlapping A or B.  tile >= 1 and count >= 0, else OM_EINVAL.  This is
+ * the kernel om_merge_i32_noalloc runs before its tile merge; om_merge_i32
+ * finds the same splitters inside its tile-merge kernel.  Allocates nothing.
+ */
+om_status om_partition_i32(const int32_t *A, int64_t m, const int32_t *B,
+                           int64_t n, int64_t tile, int64_t count,
+                           int64_t *split, void *stream);
+
+/*
  * C[0 .. m+n) = stable merge of int32 A[0..m) and B[0..n); ties take A
  * first.  One launch of the circular-buffer tile-merge kernel on `stream`:
- * each CTA first finds the co-ranks of its output range's two ends (a
- * search by the whole CTA), then merges the range.  Allocates nothing.
+ * in each CTA two warps first find the co-ranks of its output range's two
+ * ends (one each), then the CTA merges the range.  Allocates nothing.
  */
 om_status om_merge_i32(const int32_t *A, int64_t m, const int32_t *B,
                        int64_t n, int32_t *C, void *stream);
@@ -178,12 +195,14 @@ int64_t om_subtiles_per_range(int64_t segs, int64_t seg_len, int64_t subtile, in
  * reserved in full by another allocator, and code with latency bounds that
  * must not enter an allocator.
  *
- *  - m + n may be at most 1,006,510,080 (the array holds 8191 output-range
- *    splitters; ranges are lengthened as needed to fit); larger merges return
- *    OM_ERANGE and launch nothing.
- *  - The first call on each device does a one-time set-up there (it looks up
- *    the array's device address and sets kernel attributes); make that first
- *    call before any stream capture.
+ *  - m + n may be at most 2^30 = 1,073,741,824, a fixed bound of this call
+ *    (the array holds 8191 output-range splitters, and ranges are lengthened
+ *    as needed to fit); larger merges return OM_ERANGE and launch nothing.
+ *  - The first call on each device does a one-time set-up there: it looks up
+ *    the device addresses of the array and of the library's error word, sets
+ *    the merge kernels' shared-memory limits and queries their occupancy.
+ *    None of that allocates device memory (no memory pool is created; only
+ *    the sorts make one); make that first call before any stream capture.
  *  - All calls on a device share the array.  Each call's kernels write every
  *    slot they read before reading it, so nothing needs clearing, but calls
  *    whose kernels overlap on the GPU (e.g. on different streams) race on
@@ -212,9 +231,9 @@ om_status om_merge_i32_one_thread(const int32_t *A, int64_t m,
 
 /*
  * om_merge_i32_slices: one thread per slice of per_thread outputs (blocks of
- * 256 threads); each thread finds its slice's start with one co-rank search
- * in global memory, then merges the slice straight from global memory, with
- * no shared memory ("Co-rank Function 實作與 Basic Parallel Merge Kernel",
+ * 256 threads); each thread finds the co-ranks of both ends of its slice in
+ * global memory, then merges the input intervals between them straight from
+ * global memory, with no shared memory ("Co-rank Function 實作與 Basic Parallel Merge Kernel",
  * §Basic Parallel Merge Kernel; "merge_path.cu").  per_thread >= 1, else
  * OM_EINVAL.
  */

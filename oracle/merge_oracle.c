@@ -37,7 +37,10 @@
  * Parity pins: every function here is pinned by tests/test_oracle_pins.py
  * against the pages' worked example and trace, hand-derived tie cases,
  * closed forms, brute-force stable sorting of the concatenation and
- * library stable sorts.  None is "parity unpinned".
+ * library stable sorts.  The unsigned variant of O2 is pinned by brute force
+ * over keys on both sides of the sign bit and by random heavy-tie inputs,
+ * against the co-rank counted from Python's stable sort
+ * (check_corank_pages_u32).  None is "parity unpinned".
  */
 #include <stdint.h>
 #include <stdlib.h>

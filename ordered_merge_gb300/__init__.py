@@ -46,8 +46,12 @@ def _load():
     lib.om_corank_i32.restype = I64
     lib.om_corank_i32_batch.argtypes = [P, I64, P, I64, P, I64, P, P]
     lib.om_corank_i32_batch.restype = I32
+    lib.om_partition_i32.argtypes = [P, I64, P, I64, I64, I64, P, P]
+    lib.om_partition_i32.restype = I32
     lib.om_merge_i32.argtypes = [P, I64, P, I64, P, P]
     lib.om_merge_i32.restype = I32
+    lib.om_merge_i32_noalloc.argtypes = [P, I64, P, I64, P, P]
+    lib.om_merge_i32_noalloc.restype = I32
     lib.om_merge_pairs_u32.argtypes = [P, P, I64, P, P, I64, P, P, P]
     lib.om_merge_pairs_u32.restype = I32
     lib.om_merge_sort_u32.argtypes = [P, P, I64, P]
@@ -156,6 +160,28 @@ def om_corank_i32_batch(ks, A, B, out=None, stream=None):
     return out
 
 
+def om_partition_i32(A, B, tile: int, count: int | None = None, out=None, stream=None):
+    """split[t] = co_rank(min(t * tile, len(A) + len(B))) for t < count
+    (default: one per tile boundary, ceil((m + n) / tile) + 1), by the
+    partition kernel (asynchronous); j_t = min(t * tile, m + n) - split[t]."""
+    import torch
+
+    total = A.numel() + B.numel()
+    if count is None:
+        count = (total + tile - 1) // tile + 1 if tile > 0 else 0
+    if out is None:
+        out = torch.empty(count, dtype=torch.int64, device=A.device)
+    if out.dtype != torch.int64 or out.numel() != count or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int64 tensor of count elements")
+    _on_current_device(out, "out")
+    _check(
+        _lib.om_partition_i32(_ptr4(A, "A"), A.numel(), _ptr4(B, "B"), B.numel(), int(tile), int(count),
+                              out.data_ptr() if out.numel() else None, _stream(stream)),
+        "om_partition_i32",
+    )
+    return out
+
+
 def om_merge_i32(A, B, C=None, stream=None):
     """C = stable merge of sorted int32 device tensors A and B (ties: A first)."""
     import torch
@@ -167,6 +193,23 @@ def om_merge_i32(A, B, C=None, stream=None):
     _check(
         _lib.om_merge_i32(_ptr4(A, "A"), A.numel(), _ptr4(B, "B"), B.numel(), _ptr4(C, "C"), _stream(stream)),
         "om_merge_i32",
+    )
+    return C
+
+
+def om_merge_i32_noalloc(A, B, C=None, stream=None):
+    """om_merge_i32 through the entry point that allocates nothing on the
+    device (splitters in the library's fixed array; m + n <= 2^30)."""
+    import torch
+
+    if C is None:
+        C = torch.empty(A.numel() + B.numel(), dtype=torch.int32, device=A.device)
+    if C.numel() != A.numel() + B.numel():
+        raise ValueError("C must hold len(A) + len(B) elements")
+    _check(
+        _lib.om_merge_i32_noalloc(_ptr4(A, "A"), A.numel(), _ptr4(B, "B"), B.numel(), _ptr4(C, "C"),
+                                  _stream(stream)),
+        "om_merge_i32_noalloc",
     )
     return C
 
@@ -345,6 +388,8 @@ def om_subtiles_per_range(segs: int, seg_len: int, subtile: int, bytes_per_outpu
 corank_i32 = om_corank_i32
 corank_i32_batch = om_corank_i32_batch
 merge_i32 = om_merge_i32
+partition_i32 = om_partition_i32
+merge_i32_noalloc = om_merge_i32_noalloc
 merge_pairs_u32 = om_merge_pairs_u32
 merge_keys = om_merge_keys
 merge_sort_keys = om_merge_sort_keys

@@ -54,27 +54,38 @@ om_status device_state(DeviceState** out) {
         if (e != cudaSuccess) return OM_ECUDA;
         if (d.resident_merge < 1) d.resident_merge = 1;
         if (d.resident_merge_v < 1) d.resident_merge_v = 1;
-        // Scratch pool: freed scratch stays mapped for the next call, so a
-        // sort does not map and unmap its second buffer every time the
-        // caller synchronises (which a pool with the default threshold of 0
-        // would do).
+        d.dev = dev;
+        d.ready = true;
+    }
+    *out = &d;
+    return OM_OK;
+}
+
+om_status scratch_pool(DeviceState* d, cudaMemPool_t* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d->pool == nullptr) {
+        // Freed scratch stays mapped for the next call, so a sort does not
+        // map and unmap its second buffer every time the caller synchronises
+        // (which a pool with the default threshold of 0 would do).
         cudaMemPoolProps props = {};
         props.allocType = cudaMemAllocationTypePinned;
         props.handleTypes = cudaMemHandleTypeNone;
         props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+        props.location.id = d->dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
             cudaGetLastError();
             return OM_ECUDA;
         }
         uint64_t keep = UINT64_MAX;
-        if (cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
             cudaGetLastError();
+            cudaMemPoolDestroy(pool);
             return OM_ECUDA;
         }
-        d.ready = true;
+        d->pool = pool;
     }
-    *out = &d;
+    *out = d->pool;
     return OM_OK;
 }
 
@@ -254,6 +265,32 @@ om_status om_corank_i32_batch(const int64_t* ks, int64_t count, const int32_t* A
     return e == cudaSuccess ? OM_OK : OM_ECUDA;
 }
 
+om_status om_partition_i32(const int32_t* A, int64_t m, const int32_t* B, int64_t n, int64_t tile, int64_t count,
+                           int64_t* split, void* stream) {
+    if (m < 0 || n < 0 || count < 0 || tile < 1) return OM_EINVAL;
+    if (m > INT64_MAX - n) return OM_ERANGE;
+    if (count == 0) return OM_OK;
+    if (split == nullptr || misaligned(split, 8) || (m > 0 && A == nullptr) || (n > 0 && B == nullptr) ||
+        misaligned4(A) || misaligned4(B))
+        return OM_EINVAL;
+    // split counted in 4-byte units (2 per int64), like A and B
+    if (overlaps(split, 2 * count, A, m) || overlaps(split, 2 * count, B, n)) return OM_EINVAL;
+    if ((count + 3) / 4 > 0x7fffffff) return OM_ERANGE;
+    DeviceState* d = nullptr;
+    const om_status s = device_state(&d);
+    if (s != OM_OK) return s;
+    const int64_t total = m + n;
+    // tile boundaries t * tile for t < count, each clamped to m + n in the
+    // kernel; ranges_per_seg = count keeps every boundary in the one merge
+    const int64_t range_len = tile < total ? tile : (total > 0 ? total : 1);
+    MergeGeom<int32_t> g{A, nullptr, B, nullptr, nullptr, nullptr, m, n, 0, range_len, count, count};
+    cudaStream_t st = (cudaStream_t)stream;
+    const unsigned pgrid = (unsigned)((count + 3) / 4);  // one warp per boundary
+    const cudaError_t e =
+        traced(kKindPartition, st, [&] { partition_kernel<int32_t, false><<<pgrid, 128, 0, st>>>(g, split); });
+    return e == cudaSuccess ? OM_OK : OM_ECUDA;
+}
+
 om_status om_merge_i32(const int32_t* A, int64_t m, const int32_t* B, int64_t n, int32_t* C, void* stream) {
     if (m < 0 || n < 0) return OM_EINVAL;
     if (m > INT64_MAX - n) return OM_ERANGE;
@@ -413,7 +450,13 @@ om_status om_release_scratch(void) {
     const om_status s = device_state(&d);
     if (s != OM_OK) return s;
     if (cudaDeviceSynchronize() != cudaSuccess) return OM_ECUDA;
-    return cudaMemPoolTrimTo(d->pool, 0) == cudaSuccess ? OM_OK : OM_ECUDA;
+    cudaMemPool_t pool = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        pool = d->pool;
+    }
+    if (pool == nullptr) return OM_OK;  // no sort has run on this device: nothing is held
+    return cudaMemPoolTrimTo(pool, 0) == cudaSuccess ? OM_OK : OM_ECUDA;
 }
 
 // ------------------------------------------------- merge without allocating --
@@ -435,9 +478,11 @@ om_status om_release_scratch(void) {
 // cleared between calls; but two calls whose kernels overlap on the GPU (for
 // example on two streams) race on the array and may produce wrong output.
 constexpr int64_t kNoAllocSplits = 8192;  // int64 slots: 64 KiB
-// The documented limit on m + n.  Output ranges are lengthened as needed so
-// that any merge up to it needs at most kNoAllocSplits - 1 of them.
-constexpr int64_t kNoAllocMaxOutputs = 1006510080;
+// The documented limit on m + n (2^30).  It is a fixed bound of the API, not
+// a kernel limit: output ranges are lengthened as needed so that a merge of
+// any length needs at most kNoAllocSplits - 1 of them (at the limit a range
+// is 45 sub-tiles long).
+constexpr int64_t kNoAllocMaxOutputs = (int64_t)1 << 30;
 
 static __device__ __align__(256) int64_t g_noalloc_splits[kNoAllocSplits];
 

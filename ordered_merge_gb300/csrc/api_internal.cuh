@@ -100,19 +100,24 @@ struct DeviceState {
     int resident_merge_v = 0;
     uint32_t* err = nullptr;
     int64_t* corank_slot = nullptr;
-    cudaMemPool_t pool = nullptr;  // the library's scratch pool on this device
+    int dev = 0;
+    cudaMemPool_t pool = nullptr;  // the library's scratch pool on this device (made by the first sort)
 };
 
 // Per-device set-up, once per device (thread-safe): SM count, addresses of
-// the library's device words, shared-memory limits of the kernels, the
-// scratch pool.
+// the library's device words, shared-memory limits and occupancy of the
+// merge kernels.  It creates no memory pool and allocates nothing.
 om_status device_state(DeviceState** out);
 
-// Stream-ordered scratch from the library's own memory pool.  The pool keeps
-// freed memory mapped for the next call (release threshold: unlimited) until
+// The library's scratch pool on d's device, created on first use (by the
+// first call that needs scratch: a sort).  The pool keeps freed memory
+// mapped for the next call (release threshold: unlimited) until
 // om_release_scratch() trims it; the caller's default pool is not touched.
-inline cudaError_t scratch_alloc(const DeviceState* d, void** p, size_t bytes, cudaStream_t st) {
-    return cudaMallocFromPoolAsync(p, bytes, d->pool, st);
+om_status scratch_pool(DeviceState* d, cudaMemPool_t* out);
+
+// Stream-ordered scratch from that pool.
+inline cudaError_t scratch_alloc(cudaMemPool_t pool, void** p, size_t bytes, cudaStream_t st) {
+    return cudaMallocFromPoolAsync(p, bytes, pool, st);
 }
 inline cudaError_t scratch_free(void* p, cudaStream_t st) { return cudaFreeAsync(p, st); }
 
@@ -245,8 +250,11 @@ om_status sort_impl(K* keys, uint32_t* vals, int64_t n, int resident_per_sm, cud
     uint32_t* tv = nullptr;
     cudaError_t e = cudaSuccess;
     if (passes > 0) {
-        e = scratch_alloc(d, reinterpret_cast<void**>(&tk), (size_t)n * sizeof(K), st);
-        if (e == cudaSuccess && V) e = scratch_alloc(d, reinterpret_cast<void**>(&tv), (size_t)n * 4, st);
+        cudaMemPool_t pool = nullptr;
+        s = scratch_pool(d, &pool);
+        if (s != OM_OK) return s;
+        e = scratch_alloc(pool, reinterpret_cast<void**>(&tk), (size_t)n * sizeof(K), st);
+        if (e == cudaSuccess && V) e = scratch_alloc(pool, reinterpret_cast<void**>(&tv), (size_t)n * 4, st);
         if (e != cudaSuccess) {
             cudaGetLastError();
             if (tk) scratch_free(tk, st);

@@ -224,8 +224,8 @@ __global__ void __launch_bounds__(128) partition_kernel(MergeGeom<K> g, int64_t*
     const int64_t local = r - seg * g.ranges_per_seg;
     const Segment<K> s = segment_of<K, V>(g, seg);
     const int64_t len = s.m + s.n;
-    int64_t k = local * g.range_len;
-    if (k > len) k = len;
+    // local * range_len, clamped to len without overflowing
+    const int64_t k = (local > len / g.range_len) ? len : (local * g.range_len < len ? local * g.range_len : len);
     const int64_t i = corank_warp<K, DESC>(k, s.ak, s.m, s.bk, s.n, lane);
     if (lane == 0) split[r] = i;
 }

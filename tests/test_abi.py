@@ -131,3 +131,43 @@ def test_comparison_merges_host_argument_checks():
     assert L.om_merge_i32_one_thread(0x1002, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL  # misaligned
     assert L.om_merge_i32_one_thread(None, 0, None, 0, None, None) == om.OM_OK
     assert L.om_merge_i32_one_thread(0x1000, 2**62, 0x2000, 2**62, 0x3000, None) == om.OM_ERANGE
+
+
+def test_partition_and_noalloc_host_argument_checks():
+    import ordered_merge_gb300 as om
+
+    L = om.lib()
+    # partition: tile < 1, negative count or length, NULL or misaligned split, overlap with an input
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 0, 3, 0x3000, None) == om.OM_EINVAL
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 4, -1, 0x3000, None) == om.OM_EINVAL
+    assert L.om_partition_i32(0x1000, -4, 0x2000, 4, 4, 3, 0x3000, None) == om.OM_EINVAL
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 4, 0, None, None) == om.OM_OK  # nothing to do
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 4, 3, None, None) == om.OM_EINVAL
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 4, 3, 0x3004, None) == om.OM_EINVAL
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 4, 3, 0x1008, None) == om.OM_EINVAL
+    assert L.om_partition_i32(0x1002, 4, 0x2000, 4, 4, 3, 0x3000, None) == om.OM_EINVAL
+    assert L.om_partition_i32(0x1000, 2**62, 0x2000, 2**62, 4, 3, 0x3000, None) == om.OM_ERANGE
+    # no-alloc merge: the same rules as om_merge_i32, and the fixed size limit
+    assert L.om_merge_i32_noalloc(None, 0, None, 0, None, None) == om.OM_OK
+    assert L.om_merge_i32_noalloc(0x1000, -1, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+    assert L.om_merge_i32_noalloc(0x1002, 4, 0x2000, 4, 0x3000, None) == om.OM_EINVAL
+    assert L.om_merge_i32_noalloc(0x1000, 4, 0x2000, 4, 0x1008, None) == om.OM_EINVAL
+    assert L.om_merge_i32_noalloc(0x1000, (1 << 30) - 4, 0x2000, 5, 0x3000, None) == om.OM_ERANGE
+
+
+def test_partition_split_next_to_inputs_is_not_overlap():
+    """The split array is counted in 8-byte elements and the inputs in 4-byte
+    ones: a split array that starts right after A or B does not overlap them.
+    A count too large for one launch makes the call stop with OM_ERANGE just
+    after the overlap check, so nothing reaches a device."""
+    import ordered_merge_gb300 as om
+
+    L = om.lib()
+    huge = 1 << 36
+    # A = [0x1000, 0x1010) and B = [0x100, 0x110) below the split array
+    assert L.om_partition_i32(0x1000, 4, 0x100, 4, 2, huge, 0x1010, None) == om.OM_ERANGE
+    # B = [0x2000, 0x2010) and A below: split starting at B's end
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 2, huge, 0x2010, None) == om.OM_ERANGE
+    # starting inside B, or covering A: rejected as overlap
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 2, huge, 0x2008, None) == om.OM_EINVAL
+    assert L.om_partition_i32(0x1000, 4, 0x2000, 4, 2, 3, 0x0FF8, None) == om.OM_EINVAL

@@ -62,6 +62,12 @@ MUTANTS = [
     ("sort_keys_drops_B_values", "        if (vc != NULL) vc[k] = vb[j];\n    }", "    }", 0),
     ("sort_keys_stops_one_pass_early", "for (int64_t width = 1; width < n; width *= 2) {", "for (int64_t width = 2; width < n; width *= 2) {", 1),
     ("sort_stops_one_pass_early", "for (int64_t width = 1; width < n; width *= 2) {", "for (int64_t width = 2; width < n; width *= 2) {", 0),
+    ("corank_u32_signed_compare",
+     "int64_t oracle_corank_pages_u32(int64_t k, const uint32_t *A, int64_t m,\n                                const uint32_t *B, int64_t n)",
+     "int64_t oracle_corank_pages_u32(int64_t k, const int32_t *A, int64_t m,\n                                const int32_t *B, int64_t n)", 0),
+    ("corank_u32_symmetric_test", "B[j - 1] >= A[i]) {\n            int64_t delta", "B[j - 1] > A[i]) {\n            int64_t delta", 0),
+    ("corank_u32_i_too_big_on_tie", "A[i - 1] > B[j]) {\n            int64_t delta", "A[i - 1] >= B[j]) {\n            int64_t delta", 0),
+    ("corank_u32_floor_step", "int64_t delta = (i - i_low + 1) >> 1;", "int64_t delta = (i - i_low) >> 1;", 0),
 ]
 
 

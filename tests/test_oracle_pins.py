@@ -123,6 +123,38 @@ def check_brute_force(lib, max_len=5, alphabet=(0, 1, 2)):
                     a_count += tagged[k][1] == 0
 
 
+def check_corank_pages_u32(lib, max_len=4, alphabet=(0, 1, 0x7FFFFFFF, 0x80000000, 0xFFFFFFFF)):
+    """The pages' co-rank loop with unsigned compares (O2 on uint32 keys):
+    for every pair of sorted inputs up to max_len over an alphabet that
+    straddles the sign bit (where a signed compare would reorder keys), and
+    for random heavy-tie inputs over the full uint32 range, the result
+    equals the number of A tags among the first k items of Python's stable
+    sort of the tagged concatenation (the co-rank definition)."""
+    def want_coranks(A, B):
+        tagged = sorted([(a, 0) for a in A] + [(b, 1) for b in B], key=lambda t: t[0])
+        out, a_count = [0], 0
+        for _, side in tagged:
+            a_count += side == 0
+            out.append(a_count)
+        return out
+
+    seqs = [list(s) for s in _sorted_seqs(max_len, alphabet)]
+    for A in seqs:
+        for B in seqs:
+            want = want_coranks(A, B)
+            for k in range(len(A) + len(B) + 1):
+                assert oracle.corank_pages_u32(k, A, B, lib=lib) == want[k], (A, B, k)
+    rng = np.random.default_rng(17)
+    for _ in range(30):
+        m, n = (int(x) for x in rng.integers(0, 90, 2))
+        pool = rng.integers(0, 1 << 32, 6, dtype=np.uint64)  # few distinct keys: heavy ties
+        A = sorted(int(x) for x in rng.choice(pool, m))
+        B = sorted(int(x) for x in rng.choice(pool, n))
+        want = want_coranks(A, B)
+        for k in range(m + n + 1):
+            assert oracle.corank_pages_u32(k, A, B, lib=lib) == want[k], (A, B, k)
+
+
 def check_evens_odds_closed_form(lib, scale_log2=0):
     """Evens/odds workload: with n = len(B) and A = 0,2,4,... longer by t0:
     C[k] = k for k < 2n, and C[2n + t] = 2n + 2t for the A-only tail;
@@ -397,6 +429,7 @@ ALL_CHECKS = [
     check_worked_example,
     check_tie_case,
     check_brute_force,
+    check_corank_pages_u32,
     check_evens_odds_closed_form,
     check_pairs_ties_closed_form,
     check_invariants_random,
