@@ -253,10 +253,13 @@ __global__ void __launch_bounds__(128) corank_batch_kernel(const int64_t* __rest
 
 // ------------------------------------------------------------ tile merge --
 
-template <int NT_, int VT_, int RING_LOG2_, int CH_LOG2_>
+template <int NT_, int VT_, int RING_LOG2_, int CH_LOG2_, int MIN_CTAS_ = 5>
 struct TileCfg {
     static constexpr int NT = NT_;          // consumer threads
     static constexpr int THREADS = NT + 64;  // plus two producer warps
+    // CTAs per SM the shape is sized for (by its shared memory): the register
+    // budget the compiler must keep to
+    static constexpr int MIN_CTAS = MIN_CTAS_;
     static constexpr int VT = VT_;
     static constexpr int T = NT * VT;  // outputs per sub-tile
     static constexpr int RING_LOG2 = RING_LOG2_;
@@ -565,7 +568,7 @@ struct TileSmem {
 // Consumers never run a CTA-wide barrier and keep no streaming state; with
 // the next window published while they merge, they rarely wait for it.
 template <typename Cfg, typename K, bool V, bool DESC = false>
-__global__ void __launch_bounds__(Cfg::THREADS) tile_merge_kernel(MergeGeom<K> g,
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel(MergeGeom<K> g,
                                                                     const int64_t* __restrict__ split,
                                                                     uint32_t* err) {
     constexpr int NT = Cfg::NT;

@@ -228,7 +228,8 @@ def unsorted_keys(rng, name, size, span):
 
 @pytest.mark.parametrize("desc", [False, True], ids=["asc", "desc"])
 @pytest.mark.parametrize("name", TYPES)
-@pytest.mark.parametrize("n", [0, 1, 2, 17, 4095, 4096, 4097, 10000, 100003, (1 << 18) + 12345])
+@pytest.mark.parametrize("n", [0, 1, 2, 17, 18, 4095, 4096, 4351, 4352, 4353, 8705, 10000, 100003,
+                               (1 << 18) + 12345])
 def test_sort_sizes(gpu, name, desc, n):
     rng = np.random.default_rng(n + 13 * TYPES.index(name) + desc)
     check_sort(gpu, name, unsorted_keys(rng, name, n, 1 << 30), desc)

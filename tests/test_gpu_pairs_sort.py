@@ -110,7 +110,8 @@ def check_sort(om, keys, with_vals=True):
         assert np.array_equal(gv, wv), f"values differ first at {int(np.flatnonzero(gv != wv)[0])}"
 
 
-@pytest.mark.parametrize("n", [0, 1, 2, 3, 17, 1023, 1024, 1025, 2048, 4095, 4097, 8192, 10000, 65536,
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 16, 17, 18, 34, 35, 1023, 1024, 1025, 2048, 4095, 4097, 4351, 4352, 4353,
+                               8192, 8703, 8704, 8705, 10000, 13057, 65536,
                                100003, 1 << 18, (1 << 18) + 12345])
 def test_sort_sizes(gpu, n):
     rng = np.random.default_rng(n)
