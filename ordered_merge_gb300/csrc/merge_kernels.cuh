@@ -528,6 +528,39 @@ __device__ __forceinline__ uint32_t merge_serial(int a, int b, int cnt, int wa, 
 // previous sub-tile's use of its side plus this margin fits in it.
 constexpr int kPartialMargin = 128;
 
+// Whether the sub-tile's teff outputs all come from one side, decided from
+// the windows' ends alone: 1 when A's window holds teff elements and its
+// teff-th goes out no later than B's first (or B's window is empty: its
+// range is used up); 2 when the same holds for B with B strictly first;
+// 0 otherwise.  Long runs of one input (a much shorter other input, runs of
+// equal keys) give such sub-tiles; their co-rank is then teff or 0 with no
+// search, and the merge is a copy of that side's window.  A cut window is
+// never empty, so an empty window means the side has no more data.
+template <typename Cfg, typename K, bool DESC>
+__device__ __forceinline__ int one_sided(const K* ring, uint32_t ha, uint32_t hb, int wa, int wb, int teff) {
+    constexpr uint32_t M = Cfg::RMASK;
+    const K* rb = ring + Cfg::RSTRIDE;
+    if (wa >= teff && (wb == 0 || a_first<DESC>(ring[(ha + (uint32_t)teff - 1) & M], rb[hb & M]))) return 1;
+    if (wb >= teff && (wa == 0 || !a_first<DESC>(ring[ha & M], rb[(hb + (uint32_t)teff - 1) & M]))) return 2;
+    return 0;
+}
+
+// Copy of cnt (<= VT) consecutive elements of one ring window, from slot
+// `from` on, into the thread's output registers (keys and values); the
+// overhang past the ring end means the walk needs no wrap mask.
+template <typename Cfg, typename K, bool V>
+__device__ __forceinline__ void copy_window(const K* rk, const uint32_t* rv, uint32_t from, int cnt,
+                                            K (&keys)[Cfg::VT], uint32_t (&vals)[Cfg::VT]) {
+    const uint32_t p0 = from & Cfg::RMASK;
+#pragma unroll
+    for (int v = 0; v < Cfg::VT; ++v) {
+        if (v < cnt) {
+            keys[v] = rk[p0 + v];
+            if (V) vals[v] = rv[p0 + v];
+        }
+    }
+}
+
 // Shared memory of the tile-merge kernel: keys of both rings back to back
 // (A ring, then B ring, so one masked index addresses either), values
 // likewise, the output stage, the chunk barriers of both sides, the
@@ -538,7 +571,7 @@ struct TileSmem {
     static constexpr size_t stage_bytes = (size_t)Cfg::STAGE * (E + (V ? 4 : 0));
     // chunk barriers of A and B, ready[2], done[2], stage_free
     static constexpr size_t bar_bytes = (size_t)(2 * Cfg::NCH + 5) * 8;
-    // window descriptors: 2 x {ha, hb, wa, wb, teff, partial_a, partial_b, -},
+    // window descriptors: 2 x {ha, hb, wa, wb, teff, partial_a, partial_b, hint},
     // then the abort flag and padding
     static constexpr size_t info_bytes = 2 * 8 * 4 + 8 * 4;
     // the range's two co-ranks when the producer warps search them (int64 x 2)
@@ -587,7 +620,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel
     uint64_t* ready = bars_b + Cfg::NCH;  // [2]
     uint64_t* done = ready + 2;          // [2]
     uint64_t* stage_free = done + 2;     // [1]
-    int* info = reinterpret_cast<int*>(stage_free + 1);  // [2][8]: ha, hb, wa, wb, teff, partial a/b
+    int* info = reinterpret_cast<int*>(stage_free + 1);  // [2][8]: ha, hb, wa, wb, teff, partial a/b, hint
     volatile int* abort_flag = info + 20;
     int64_t* bound_slot = reinterpret_cast<int64_t*>(smem + Smem::ring_bytes + Smem::stage_bytes +
                                                      Smem::bar_bytes + Smem::info_bytes);  // [2]
@@ -685,8 +718,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel
         // before the sub-tile counts.  early: publishing before the previous
         // sub-tile's consumers are done, from data already requested; returns
         // 0 when that data cannot serve, 1 when published, -1 on a timeout.
+        //
+        // hint: whether the consumers should test the sub-tile for being
+        // one-sided (one_sided): set after a sub-tile whose outputs all came
+        // from one side (a run of one side usually goes on), and for the
+        // first and any redone sub-tile.  Interleaved data then never pays
+        // for the test; a run that starts inside a sub-tile is merged there
+        // and copied from the next sub-tile on.
         auto publish = [&](int it, int64_t kd, int64_t head, int64_t avail_chunk, int prev_used, bool force_full,
-                           bool early) -> int {
+                           bool early, int hint) -> int {
             const int teff = (int)((kend - kd) < T ? (kend - kd) : T);
             int* inf = info + 8 * (it & 1);
             if (teff == 0) {  // every sub-tile is merged: tell the consumers to stop
@@ -712,13 +752,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel
             inf[side_a ? 0 : 1] = (int)((uint32_t)head & Cfg::RMASK);
             inf[side_a ? 2 : 3] = w;
             inf[side_a ? 5 : 6] = partial;
-            if (side_a) inf[4] = teff;
+            if (side_a) {
+                inf[4] = teff;
+                inf[7] = hint;
+            }
             if (!ok) *abort_flag = 1;
             mbar_arrive(&ready[it & 1]);  // release: this side's window and descriptor
             return ok ? 1 : -1;
         };
 
-        if (publish(0, kdone, S.head, S.c_first, -1, true, false) < 0) failed = true;
+        if (publish(0, kdone, S.head, S.c_first, -1, true, false, 1) < 0) failed = true;
         for (int it = 0; !failed; ++it) {
             // Sub-tile `it` is published; the consumers may be merging it.
             const int teff = (int)((kend - kdone) < T ? (kend - kdone) : T);
@@ -739,11 +782,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel
             // windows, so r is the true co-rank); otherwise the sub-tile is
             // merged again with whole windows.  This runs while the consumers
             // merge.
+            // When the hint asks for it, a one-sided sub-tile (one_sided) is
+            // recognised here exactly as the consumers recognise it: it needs
+            // no search, they copy it, and it is exact whatever the windows
+            // were cut to.
             const int wa_ = inf[2], wb_ = inf[3];
-            const int r = corank_ring<Cfg, K, DESC>(teff, teff - wb_ > 0 ? teff - wb_ : 0, teff < wa_ ? teff : wa_,
-                                                    ring, (uint32_t)inf[0], (uint32_t)inf[1]);
-            const bool redo = (inf[5] | inf[6]) && !(r < wa_ && teff - r < wb_);
+            const int side =
+                inf[7] ? one_sided<Cfg, K, DESC>(ring, (uint32_t)inf[0], (uint32_t)inf[1], wa_, wb_, teff) : 0;
+            const int r = side == 1   ? teff
+                          : side == 2 ? 0
+                                      : corank_ring<Cfg, K, DESC>(teff, teff - wb_ > 0 ? teff - wb_ : 0,
+                                                                  teff < wa_ ? teff : wa_, ring, (uint32_t)inf[0],
+                                                                  (uint32_t)inf[1]);
+            const bool redo = side == 0 && (inf[5] | inf[6]) && !(r < wa_ && teff - r < wb_);
             const int used = side_a ? r : teff - r;
+            const int hint = (r == teff || r == 0) ? 1 : 0;
             // This producer has read the windows: `done` (which both refills
             // wait for) may now complete, so no refill overwrites a window
             // slot that the other producer is still searching.
@@ -752,7 +805,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel
             // that the consumers find it ready when they finish this one.
             int next = 0;
             if (!redo) {
-                next = publish(it + 1, kdone + teff, S.head + used, S.next_issue, used, false, true);
+                next = publish(it + 1, kdone + teff, S.head + used, S.next_issue, used, false, true, hint);
                 if (next < 0) {
                     failed = true;
                     break;
@@ -764,7 +817,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel
                 break;
             }
             if (redo) {  // same sub-tile again, with whole windows; nothing stored
-                if (publish(it + 1, kdone, S.head, S.next_issue, -1, true, false) < 0) failed = true;
+                if (publish(it + 1, kdone, S.head, S.next_issue, -1, true, false, 1) < 0) failed = true;
                 continue;
             }
             S.head += used;
@@ -796,7 +849,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel
                 bulk_commit();
             }
             kdone += teff;
-            if (next == 0 && publish(it + 1, kdone, S.head, first_new, used, false, false) < 0) failed = true;
+            if (next == 0 && publish(it + 1, kdone, S.head, first_new, used, false, false, hint) < 0) failed = true;
         }
         if (failed) {
             // Let every requested chunk land (bounded) before the CTA's shared
@@ -830,8 +883,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS) tile_merge_kernel
         K keys[VT];
         uint32_t vals[VT];
         const bool full = (teff == T) && (wa == T) && (wb == T);
+        const int side = inf[7] ? one_sided<Cfg, K, DESC>(ring, ha, hb, wa, wb, teff) : 0;
         int cnt = VT;
-        if (full) {
+        if (side != 0) {
+            // every output of the sub-tile comes from one side: copy it
+            cnt = (teff - d < VT) ? teff - d : VT;
+            if (side == 1) {
+                copy_window<Cfg, K, V>(ring, vring, ha + (uint32_t)d, cnt, keys, vals);
+            } else {
+                copy_window<Cfg, K, V>(ring + Cfg::RSTRIDE, V ? vring + Cfg::RSTRIDE : nullptr, hb + (uint32_t)d,
+                                       cnt, keys, vals);
+            }
+        } else if (full) {
             const int a = corank_ring<Cfg, K, DESC>(d, 0, d, ring, ha, hb);
             merge_serial<Cfg, K, V, false, DESC>(a, d - a, VT, wa, wb, ring, vring, ha, hb, keys, vals);
         } else if (partial) {
