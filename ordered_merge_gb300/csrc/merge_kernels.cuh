@@ -192,11 +192,36 @@ __device__ __forceinline__ int64_t corank_global(int64_t k, const K* __restrict_
 // dependent loads.  Every lane returns the result.  On unsorted input the
 // passing probes need not form a prefix; the interval still shrinks every
 // round, so the loop always ends.
+//
+// The first round probes a ladder around the proportional estimate
+// e = k * m / (m + n) instead (e -+ 1, 4, 16, ..., 4^15, clamped into the
+// interval): on sorted data whose two inputs mix evenly the co-rank sits
+// within a few hundred or thousand places of e, so one round brackets it
+// tightly and the 33-way rounds start from a small interval (2-3 rounds
+// fewer on large inputs).  Any sorted list of probes in (lo, hi] keeps the
+// search exact: the passing probes are a prefix, and the interval becomes
+// the gap between the last passing and the first failing one.
 template <typename K, bool DESC = false>
 __device__ __forceinline__ int64_t corank_warp(int64_t k, const K* __restrict__ A, int64_t m,
                                                const K* __restrict__ B, int64_t n, int lane) {
     int64_t lo = k - n > 0 ? k - n : 0;
     int64_t hi = k < m ? k : m;
+    if (hi - lo > 64) {
+        const int64_t e = (int64_t)((double)k * (double)m / (double)(m + n));
+        const int j = lane < 16 ? 15 - lane : lane - 16;  // ladder step 4^j
+        const int64_t off = (int64_t)1 << (2 * j);
+        int64_t c = lane < 16 ? e - off + 1 : e + off;   // e-4^15+1 .. e, e+1 .. e+4^15
+        c = c <= lo ? lo + 1 : (c > hi ? hi : c);        // sorted, in (lo, hi]
+        const bool pass = a_first<DESC>(__ldg(A + c - 1), __ldg(B + k - c));
+        const unsigned bal = __ballot_sync(0xffffffffu, pass);
+        const int t = __popc(bal);
+        const int64_t c_prev = __shfl_sync(0xffffffffu, c, t > 0 ? t - 1 : 0);
+        const int64_t c_next = __shfl_sync(0xffffffffu, c, t < 32 ? t : 31);
+        const int64_t new_lo = t == 0 ? lo : c_prev;
+        const int64_t new_hi = t == 32 ? hi : c_next - 1;
+        lo = new_lo;
+        hi = new_hi > lo ? new_hi : lo;  // (on unsorted input the probes need not form a prefix)
+    }
     while (hi - lo > 32) {
         const int64_t span = hi - lo;
         const int64_t c = lo + (span * (lane + 1)) / 33;  // lo < c < hi

@@ -117,13 +117,13 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // Waits until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Plain arrive (count 1) on `bar`.
 // Barrier `id` (1..15; 0 is __syncthreads) among `count` threads (a
 // multiple of 32, whole warps).
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Plain arrive (count 1) on `bar`.
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
