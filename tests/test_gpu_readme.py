@@ -25,6 +25,10 @@ def test_readme_example(gpu):
     A, B, C = (ns[k].cpu().numpy() for k in ("A", "B", "C"))
     assert np.array_equal(C, oracle.merge_i32(A, B))
     assert ns["i"] == oracle.corank_count(12345, A, B)
+    split = ns["split"].cpu().numpy()
+    assert split.size == (A.size + B.size + 4095) // 4096 + 1
+    for t in [0, 1, 2, split.size // 2, split.size - 1]:
+        assert split[t] == oracle.corank_pages(min(t * 4096, A.size + B.size), A, B)
     X, Y, Z = (ns[k].cpu().numpy() for k in ("X", "Y", "Z"))
     assert np.array_equal(Z.view(np.uint64), oracle.merge_keys(X, Y, descending=True).view(np.uint64))
     keys, vals = ns["keys"].cpu().numpy().view(np.uint32), ns["vals"].cpu().numpy().view(np.uint32)
