@@ -99,9 +99,17 @@ om_status om_partition_i32(const int32_t *A, int64_t m, const int32_t *B,
 
 /*
  * C[0 .. m+n) = stable merge of int32 A[0..m) and B[0..n); ties take A
- * first.  One launch of the circular-buffer tile-merge kernel on `stream`:
- * in each CTA two warps first find the co-ranks of its output range's two
- * ends (one each), then the CTA merges the range.  Allocates nothing.
+ * first.  One launch on `stream`.  A merge that fits in one wave of small
+ * CTAs (about 4.2 M outputs on a 152-SM GB300; the one-pass kernel: one
+ * output tile per CTA, both windows loaded into shared memory at once and
+ * merged by every thread) takes that kernel; a larger one takes the
+ * circular-buffer tile-merge kernel, whose CTAs stream their output ranges
+ * through shared-memory rings.  In either, two warps of each CTA first find
+ * the co-ranks of its output range's two ends (one each).  Allocates
+ * nothing.  The environment variable OM_ONE_PASS_MAX (an output count; 0:
+ * never) moves the size at which the one-pass kernel stops; setting
+ * OM_SUBTILES_PER_RANGE or OM_WAVES selects the tile-merge kernel.  The same
+ * holds for om_merge_pairs_u32 and om_merge_keys.
  */
 om_status om_merge_i32(const int32_t *A, int64_t m, const int32_t *B,
                        int64_t n, int32_t *C, void *stream);
@@ -145,8 +153,8 @@ om_status om_device_error(void *stream, uint32_t *detail);
 /*
  * With tracing on, every kernel launch is bracketed by two CUDA events on its
  * stream.  om_trace_read synchronises those events and returns, for kernel
- * kind `kind` (0 = partition, 1 = tile merge, 2 = block sort / small merge,
- * 3 = co-rank batch, 4 = the comparison merges below), the number of
+ * kind `kind` (0 = partition, 1 = tile merge, 2 = block sort, 3 = co-rank
+ * batch, 4 = the comparison merges below, 5 = one-pass merge), the number of
  * launches and their summed duration in milliseconds since the last
  * om_trace_reset.
  */

@@ -21,7 +21,7 @@ from .build import LIB_PATH
 
 OM_OK, OM_EINVAL, OM_ERANGE, OM_ENOMEM, OM_ECUDA, OM_EDEVICE = range(6)
 
-KIND_PARTITION, KIND_TILE_MERGE, KIND_BLOCK_SORT, KIND_CORANK, KIND_BASELINE = range(5)
+KIND_PARTITION, KIND_TILE_MERGE, KIND_BLOCK_SORT, KIND_CORANK, KIND_BASELINE, KIND_ONE_PASS = range(6)
 
 # om_key_type codes and their element sizes
 KEY_TYPES = {"i32": (0, 4), "u32": (1, 4), "f32": (2, 4), "i64": (3, 8), "u64": (4, 8), "f64": (5, 8)}

@@ -171,6 +171,16 @@ static int64_t env_int(const char* name, int64_t fallback) {
     return (end != s && v > 0) ? (int64_t)v : fallback;
 }
 
+// An output count from the environment (0 allowed), or fallback when unset
+// or not a number.
+int64_t env_outputs(const char* name, int64_t fallback) {
+    const char* s = std::getenv(name);
+    if (s == nullptr || *s == 0) return fallback;
+    char* end = nullptr;
+    const long long v = std::strtoll(s, &end, 10);
+    return (end != s && v >= 0) ? (int64_t)v : fallback;
+}
+
 // Sub-tiles per CTA output range for one launch over `segs` independent
 // merges of at most `seg_len` outputs each (a merge: one segment; a late
 // pass of the sort: one segment per pair of runs).  A range never crosses a

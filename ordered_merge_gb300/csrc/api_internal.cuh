@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "merge_kernels.cuh"
+#include "one_pass_merge.cuh"
 #include "ordmerge.h"
 #include "sort_kernels.cuh"
 
@@ -74,6 +75,15 @@ using SmemOf = TileSmem<Cfg, V, KeyGeom<K>::E>;
 template <typename K, bool V>
 using SmemFor = SmemOf<typename CfgFor<K, V>::type, K, V>;
 
+// One-pass tile shape of a merge of K keys (with values when V), for merges
+// that fit in one wave of it: 128 threads, 8 CTAs per SM (64 registers a
+// thread).  4-byte keys alone merge 27 outputs a thread (one wave of 152 x 8
+// CTAs covers 4.2 M outputs); keys with values, and 8-byte keys, 15.
+template <typename K, bool V>
+struct OnePassFor {
+    using type = OnePassCfg<128, (sizeof(K) == 4 && !V) ? 27 : 15, 8>;
+};
+
 //  sort: one block pass sorts 256 x 16 = 4096-element tiles in shared memory
 //        (runs of 16 in registers, then merges of whole pairs of runs per
 //        CTA up to 4096); later passes use the tile-merge kernel on each
@@ -88,7 +98,8 @@ enum KernelKind {
     kKindBlockSort = 2,
     kKindCorank = 3,
     kKindBaseline = 4,
-    kNumKinds = 5
+    kKindOnePass = 5,
+    kNumKinds = 6
 };
 
 // ------------------------------------------------------------ device state --
@@ -191,9 +202,47 @@ cudaError_t launch_merge(const MergeGeom<K>& g, int64_t* split, const DeviceStat
     });
 }
 
-// One merge of A[0..m) and B[0..n) into C (values optional): one tile-merge
-// launch whose CTAs find their own co-ranks; nothing is allocated.
-// `resident_per_sm`: tile-merge CTAs of this instantiation resident per SM.
+// Outputs one wave of the one-pass kernel covers on the current device (its
+// shared-memory limit set and its occupancy queried once per device), or 0
+// when the query fails.  The environment variable OM_ONE_PASS_MAX replaces it
+// (0: never take the one-pass path); OM_SUBTILES_PER_RANGE or OM_WAVES (the
+// tile-merge launch planning) set to a positive value means the ring kernel
+// is wanted, so the result is then 0 unless OM_ONE_PASS_MAX says otherwise.
+int64_t env_outputs(const char* name, int64_t fallback);
+
+template <typename K, bool V, bool DESC>
+int64_t one_pass_capacity(const DeviceState* d) {
+    const int64_t forced = env_outputs("OM_ONE_PASS_MAX", -1);
+    if (forced >= 0) return forced;
+    if (env_outputs("OM_SUBTILES_PER_RANGE", 0) > 0 || env_outputs("OM_WAVES", 0) > 0) return 0;
+    using OP = typename OnePassFor<K, V>::type;
+    static std::mutex mu;
+    static int resident[128];  // CTAs per SM, per device; 0 = not asked yet, -1 = unusable
+    std::lock_guard<std::mutex> lk(mu);
+    int& r = resident[d->dev & 127];
+    if (r == 0) {
+        auto* kern = one_pass_merge_kernel<OP, K, V, DESC>;
+        int blocks = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)one_pass_smem_bytes<OP, K, V>()) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, OP::NT, one_pass_smem_bytes<OP, K, V>()) !=
+                cudaSuccess ||
+            blocks < 1) {
+            cudaGetLastError();
+            r = -1;
+        } else {
+            r = blocks;
+        }
+    }
+    return r > 0 ? (int64_t)r * d->sm_count * OP::T : 0;
+}
+
+// One merge of A[0..m) and B[0..n) into C (values optional); nothing is
+// allocated.  A merge that fits in one wave of the one-pass kernel takes it
+// (one tile per CTA, merged at once); a larger one takes one tile-merge
+// launch whose CTAs stream their output ranges through the rings.  Either
+// way each CTA finds its own co-ranks.  `resident_per_sm`: tile-merge CTAs
+// of this instantiation resident per SM.
 template <typename K, bool V, bool DESC = false>
 om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, const uint32_t* bv, int64_t n, K* ck,
                      uint32_t* cv, int resident_per_sm, cudaStream_t st) {
@@ -202,6 +251,16 @@ om_status merge_impl(const K* ak, const uint32_t* av, int64_t m, const K* bk, co
     if (s != OM_OK) return s;
     using Cfg = typename CfgFor<K, V>::type;
     const int64_t total = m + n;
+    if (total <= one_pass_capacity<K, V, DESC>(d)) {
+        using OP = typename OnePassFor<K, V>::type;
+        const int64_t ntiles = (total + OP::T - 1) / OP::T;
+        MergeGeom<K> g{ak, av, bk, bv, ck, cv, m, n, 0, OP::T, ntiles, ntiles};
+        const cudaError_t e = traced(kKindOnePass, st, [&] {
+            one_pass_merge_kernel<OP, K, V, DESC>
+                <<<(unsigned)ntiles, OP::NT, one_pass_smem_bytes<OP, K, V>(), st>>>(g, d->err);
+        });
+        return e == cudaSuccess ? OM_OK : cuda_fail(e);
+    }
     const int64_t resident = (int64_t)d->sm_count * (resident_per_sm > 0 ? resident_per_sm : 1);
     const int64_t range_len = subtiles_per_range(1, total, Cfg::T, bytes_per_output<K, V>(), resident) * Cfg::T;
     const int64_t nranges = (total + range_len - 1) / range_len;

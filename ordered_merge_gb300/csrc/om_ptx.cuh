@@ -106,6 +106,21 @@ __device__ __forceinline__ void bulk_copy_s2g(void* dst_gmem, const void* src_sm
                  : "memory");
 }
 
+// Asynchronous copy of one 4- or 8-byte element from global to shared
+// memory (the thread continues; see cp_async_wait_all).
+template <int BYTES>
+__device__ __forceinline__ void cp_async_elem(void* dst_smem, const void* src_gmem) {
+    static_assert(BYTES == 4 || BYTES == 8, "4- or 8-byte elements");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_addr(dst_smem)), "l"(src_gmem),
+                 "n"(BYTES)
+                 : "memory");
+}
+
+// Waits until every cp.async of this thread has landed in shared memory.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until every committed bulk group of this thread has finished

@@ -45,3 +45,15 @@ def gpu():
     import ordered_merge_gb300 as om
 
     return om
+
+
+@pytest.fixture(params=["default", "ring"])
+def merge_path(request, monkeypatch):
+    """Runs a merge test twice: with the library's own choice of kernel
+    (merges that fit in one wave take the one-pass kernel) and with the
+    circular-buffer tile-merge kernel forced for every size."""
+    if request.param == "ring":
+        monkeypatch.setenv("OM_ONE_PASS_MAX", "0")
+    else:
+        monkeypatch.delenv("OM_ONE_PASS_MAX", raising=False)
+    return request.param

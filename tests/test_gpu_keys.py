@@ -15,7 +15,7 @@ import torch
 
 import oracle
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("merge_path")]
 
 TYPES = ["i32", "u32", "f32", "i64", "u64", "f64"]
 NP = {"i32": np.int32, "u32": np.uint32, "f32": np.float32, "i64": np.int64, "u64": np.uint64, "f64": np.float64}

@@ -14,7 +14,7 @@ import oracle
 import synth
 from gpu_util import dev_i32, guarded_empty, guards_intact, host, shifted
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("merge_path")]
 
 
 def run_merge(om, A_np, B_np, offs=(0, 0, 0)):
@@ -189,3 +189,34 @@ def test_unsorted_input_terminates_in_bounds(gpu, m, n):
     torch.cuda.synchronize()
     assert gpu.device_error() in (0, 2), "a kernel wait timed out on unsorted input"
     assert guards_intact(buf, total), "merge wrote outside C"
+
+
+def test_one_pass_path_taken_and_matches_oracle(gpu, monkeypatch):
+    """A merge that fits in one wave takes the one-pass kernel (traced as its
+    own kind) and a larger one the tile-merge kernel; both give the oracle's
+    result, at tile boundaries of the one-pass shape (3456 outputs a CTA for
+    int32) and around them."""
+    monkeypatch.delenv("OM_ONE_PASS_MAX", raising=False)
+    rng = np.random.default_rng(21)
+    for total in [1, 3455, 3456, 3457, 2 * 3456, 3456 * 40 + 17, 1 << 20]:
+        m = total // 3
+        A = np.sort(rng.integers(-1000, 1000, m)).astype(np.int32)
+        B = np.sort(rng.integers(-1000, 1000, total - m)).astype(np.int32)
+        gpu.om_trace_reset()
+        gpu.om_trace_enable(True)
+        C = gpu.merge_i32(dev_i32(A), dev_i32(B))
+        torch.cuda.synchronize()
+        gpu.om_trace_enable(False)
+        one_pass, _ = gpu.om_trace_read(gpu.KIND_ONE_PASS)
+        tile, _ = gpu.om_trace_read(gpu.KIND_TILE_MERGE)
+        assert (one_pass, tile) == (1, 0), (total, one_pass, tile)
+        assert np.array_equal(host(C), oracle.merge_i32(A, B)), total
+    # forced off: the same merge through the tile-merge kernel
+    monkeypatch.setenv("OM_ONE_PASS_MAX", "0")
+    gpu.om_trace_reset()
+    gpu.om_trace_enable(True)
+    C = gpu.merge_i32(dev_i32(A), dev_i32(B))
+    torch.cuda.synchronize()
+    gpu.om_trace_enable(False)
+    assert gpu.om_trace_read(gpu.KIND_ONE_PASS)[0] == 0 and gpu.om_trace_read(gpu.KIND_TILE_MERGE)[0] == 1
+    assert np.array_equal(host(C), oracle.merge_i32(A, B))

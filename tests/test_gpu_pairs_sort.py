@@ -8,7 +8,7 @@ import oracle
 import synth
 from gpu_util import dev_i32, guarded_empty, guards_intact, host, shifted
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("merge_path")]
 
 
 def run_pairs(om, ka, va, kb, vb, offs=(0, 0, 0)):
