@@ -58,9 +58,11 @@ WORKLOADS = {
 }
 SORTS = ("sort", "sort_f32_desc", "sort_f64")
 
-# Source files whose change invalidates a recorded ncu traffic figure.
+# Source files whose change invalidates a recorded ncu traffic figure (the
+# tile-merge and one-pass merge kernels).
 KERNEL_SOURCES = [
     "ordered_merge_gb300/csrc/merge_kernels.cuh",
+    "ordered_merge_gb300/csrc/one_pass_merge.cuh",
     "ordered_merge_gb300/csrc/sort_kernels.cuh",
     "ordered_merge_gb300/csrc/om_ptx.cuh",
     "ordered_merge_gb300/csrc/api_internal.cuh",
