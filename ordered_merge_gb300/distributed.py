@@ -259,9 +259,8 @@ def sample_sort_u32(keys_local: torch.Tensor, vals_local: torch.Tensor, group=No
     pos = sorted({(j * n) // (s + 1) for j in range(1, s + 1)} if n else set())
     pos = [p for p in pos if p < n]
     sk = [x & 0xFFFFFFFF for x in keys[torch.tensor(pos, dtype=torch.int64, device=keys.device)].tolist()] if pos else []
-    mine = torch.full((s, 3), -1, dtype=torch.int64, device=dev)
-    for t, (p, k) in enumerate(zip(pos, sk)):
-        mine[t, 0], mine[t, 1], mine[t, 2] = k, rank, p
+    rows = [[k, rank, p] for p, k in zip(pos, sk)] + [[-1, -1, -1]] * (s - len(pos))  # -1 rows: no sample
+    mine = torch.tensor(rows, dtype=torch.int64, device=dev)
     gathered = [torch.empty_like(mine) for _ in range(world)]
     dist.all_gather(gathered, mine, group=group)
     samples = sorted(tuple(int(x) for x in row) for g in gathered for row in g.cpu().tolist() if row[0] >= 0)

@@ -220,3 +220,33 @@ def test_one_pass_path_taken_and_matches_oracle(gpu, monkeypatch):
     gpu.om_trace_enable(False)
     assert gpu.om_trace_read(gpu.KIND_ONE_PASS)[0] == 0 and gpu.om_trace_read(gpu.KIND_TILE_MERGE)[0] == 1
     assert np.array_equal(host(C), oracle.merge_i32(A, B))
+
+
+@pytest.mark.parametrize("total", [1919, 1920, 1921, 2 * 1920, 1920 * 7 + 3])
+def test_one_pass_pairs_and_wide_keys_at_tile_edges(gpu, monkeypatch, total):
+    """Key+value merges and 8-byte keys take the one-pass kernel with 1920
+    outputs a CTA: outputs around that tile edge match the oracle (values
+    travel with their keys; float64 descending with -0.0 / +0.0 ties)."""
+    monkeypatch.delenv("OM_ONE_PASS_MAX", raising=False)
+    rng = np.random.default_rng(total)
+    m = total // 2 + 7
+    n = total - m
+    ka = np.sort(rng.integers(0, 9, m)).astype(np.uint32)
+    kb = np.sort(rng.integers(0, 9, n)).astype(np.uint32)
+    va = np.arange(m, dtype=np.uint32)
+    vb = (np.arange(n) | (1 << 31)).astype(np.uint32)
+    d = lambda x: torch.from_numpy(x.view(np.int32)).cuda()
+    gpu.om_trace_reset()
+    gpu.om_trace_enable(True)
+    kc, vc = gpu.merge_pairs_u32(d(ka), d(va), d(kb), d(vb))
+    torch.cuda.synchronize()
+    gpu.om_trace_enable(False)
+    assert gpu.om_trace_read(gpu.KIND_ONE_PASS)[0] == 1
+    wk, wv = oracle.merge_pairs_u32(ka, va, kb, vb)
+    assert np.array_equal(host(kc).view(np.uint32), wk)
+    assert np.array_equal(host(vc).view(np.uint32), wv)
+    fa = np.sort(rng.choice(np.array([-2.0, -0.0, 0.0, 1.5]), m))[::-1].copy()
+    fb = np.sort(rng.choice(np.array([-2.0, 0.0, -0.0, 3.0]), n))[::-1].copy()
+    fc = gpu.merge_keys(torch.from_numpy(fa).cuda(), torch.from_numpy(fb).cuda(), descending=True)
+    want = oracle.merge_keys(fa, fb, descending=True)
+    assert np.array_equal(host(fc).view(np.uint64), want.view(np.uint64))
