@@ -12,8 +12,10 @@ rank 0.
   value      merged elements/s over the K timed steps (CUDA events on the
              launching stream; max over ranks for N > 1, times N replicas)
   roofline   the tile-merge kernel: algorithmic bytes per launch
-             ((m+n) * (4 read + 4 written)) / its mean launch time (events
-             around each launch), against the measured HBM copy peak
+             ((m+n) * (4 read + 4 written)) / its mean launch time (the
+             library's launch trace: events around each launch, recorded in a
+             second pass over the same K steps, so that the call times above
+             carry no trace events), against the measured HBM copy peak
   e2e        the same metric with the host<->device copies inside the timed
              region: pinned host A, B -> device, merge, device C -> pinned host
   cpu_baseline  the CPU oracle (single thread) on the same workload
@@ -360,47 +362,37 @@ def measure(wl: str, args, device, world: int, steps: int, warmup: int, keep: bo
         torch.cuda.synchronize(device)
         if om.device_error() != 0:
             raise RuntimeError("device error during warm-up")
-        barrier(world, device)
-        torch.cuda.synchronize(device)
-        om.om_trace_reset()
-        om.om_trace_enable(True)
-        launches0 = om.om_launch_count()
-        with ClockSampler(device.index) as clk:
+
+        def timed_loop(count):
             if flush is None:
                 ev0 = torch.cuda.Event(enable_timing=True)
                 ev1 = torch.cuda.Event(enable_timing=True)
                 ev0.record(stream)
-                for _ in range(steps):
+                for _ in range(count):
                     step()
                 ev1.record(stream)
                 torch.cuda.synchronize(device)
-                ms = ev0.elapsed_time(ev1)
-            else:
-                pairs = []
-                for _ in range(steps):
-                    flush()
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    step()
-                    e1.record(stream)
-                    pairs.append((e0, e1))
-                torch.cuda.synchronize(device)
-                ms = sum(a.elapsed_time(b) for a, b in pairs)
-        launches = om.om_launch_count() - launches0
-        om.om_trace_enable(False)
+                return ev0.elapsed_time(ev1)
+            pairs = []
+            for _ in range(count):
+                flush()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                step()
+                e1.record(stream)
+                pairs.append((e0, e1))
+            torch.cuda.synchronize(device)
+            return sum(a.elapsed_time(b) for a, b in pairs)
     else:
         for _ in range(warmup):
             sort_once()
             sort_call()
         torch.cuda.synchronize(device)
-        barrier(world, device)
-        om.om_trace_reset()
-        om.om_trace_enable(True)
-        launches0 = om.om_launch_count()
-        ms = 0.0
-        with ClockSampler(device.index) as clk:
-            for _ in range(steps):
+
+        def timed_loop(count):
+            total_ms = 0.0
+            for _ in range(count):
                 sort_once()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
@@ -408,8 +400,22 @@ def measure(wl: str, args, device, world: int, steps: int, warmup: int, keep: bo
                 sort_call()
                 e1.record(stream)
                 e1.synchronize()
-                ms += e0.elapsed_time(e1)
+                total_ms += e0.elapsed_time(e1)
+            return total_ms
+
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index) as clk:
+        # the calls as a user makes them (the library's launch trace off) ...
+        launches0 = om.om_launch_count()
+        ms = timed_loop(steps)
         launches = om.om_launch_count() - launches0
+        # ... then the same loop once more with the launch trace on, for the
+        # kernels' own durations (its events sit around every launch, so the
+        # call time is not taken from this loop)
+        om.om_trace_reset()
+        om.om_trace_enable(True)
+        timed_loop(steps)
         om.om_trace_enable(False)
     if om.device_error() != 0:
         raise RuntimeError("device error during the timed region")
