@@ -200,14 +200,19 @@ __device__ __forceinline__ int64_t corank_global(int64_t k, const K* __restrict_
 // tightly and the 33-way rounds start from a small interval (2-3 rounds
 // fewer on large inputs).  Any sorted list of probes in (lo, hi] keeps the
 // search exact: the passing probes are a prefix, and the interval becomes
-// the gap between the last passing and the first failing one.
+// the gap between the last passing and the first failing one.  So e needs no
+// exactness and is taken in fp32 (relative error about 2^-23, a few places
+// on a 2^29-output merge): this GPU's FP64 rate is a small fraction of its
+// FP32 rate, and a double division in every lane of every searching warp
+// cost the one-wave merge about 1.7 us at its start.
 template <typename K, bool DESC = false>
 __device__ __forceinline__ int64_t corank_warp(int64_t k, const K* __restrict__ A, int64_t m,
                                                const K* __restrict__ B, int64_t n, int lane) {
     int64_t lo = k - n > 0 ? k - n : 0;
     int64_t hi = k < m ? k : m;
     if (hi - lo > 64) {
-        const int64_t e = (int64_t)((double)k * (double)m / (double)(m + n));
+        // 0 <= e <= about k (m + n > 0 here); the clamp below keeps every probe in (lo, hi]
+        const int64_t e = (int64_t)((float)k * __fdividef((float)m, (float)(m + n)));
         const int j = lane < 16 ? 15 - lane : lane - 16;  // ladder step 4^j
         const int64_t off = (int64_t)1 << (2 * j);
         int64_t c = lane < 16 ? e - off + 1 : e + off;   // e-4^15+1 .. e, e+1 .. e+4^15
