@@ -124,6 +124,33 @@ def test_corank_against_oracle(gpu):
             assert gpu.corank_i32(int(k), dA, dB) == oracle.corank_count(int(k), A, B)
 
 
+@pytest.mark.parametrize("m,n,layout", [(65, 3_000_001, "mixed"), (3_000_001, 65, "mixed"),
+                                        (1_500_000, 1_500_000, "a_below"), (1_500_000, 1_500_000, "b_below"),
+                                        (2_000_003, 999, "a_below"), (999, 2_000_003, "b_below"),
+                                        (70, 70, "a_below"), (70, 70, "b_below")])
+def test_corank_far_from_proportional_estimate(gpu, m, n, layout):
+    """The warp range search opens with probes around e = k m / (m + n),
+    computed in single precision; it stays exact where the co-rank lies far
+    from e (one input wholly before the other) and at extreme size ratios,
+    through om_corank_i32 and through the merge's own range searches."""
+    rng = np.random.default_rng(m * 31 + n + len(layout))
+    if layout == "mixed":
+        A = sorted_rand(rng, m, -2**31, 2**31)
+        B = sorted_rand(rng, n, -2**31, 2**31)
+    else:
+        low = (-2**31, -1)
+        high = (0, 2**31 - 1)
+        A = sorted_rand(rng, m, *(low if layout == "a_below" else high))
+        B = sorted_rand(rng, n, *(high if layout == "a_below" else low))
+    dA, dB = dev_i32(A), dev_i32(B)
+    total = m + n
+    ks = np.unique(np.concatenate([[0, 1, 64, 65, min(m, n), max(m, n), total // 2, total - 1, total],
+                                   rng.integers(0, total + 1, 40)]))
+    for k in ks:
+        assert gpu.corank_i32(int(k), dA, dB) == oracle.corank_pages(int(k), A, B), int(k)
+    check(gpu, A, B)
+
+
 def test_merge_on_side_stream(gpu):
     rng = np.random.default_rng(12)
     A, B = sorted_rand(rng, 100000, 0, 1000), sorted_rand(rng, 90000, 0, 1000)
