@@ -356,6 +356,7 @@ def measure(wl: str, args, device, world: int, steps: int, warmup: int, keep: bo
     # fit twice in L2 gets L2 flushed before every step (a write larger than
     # L2, outside the timed events); larger ones stream back to back.
     flush = L2Flusher(device) if total * bytes_per_elem < 2 * L2Flusher.l2_bytes(device) else None
+    per_step = []  # per-call times where each call is timed alone (flushed merges, sorts)
     if step is not None:
         for _ in range(warmup):
             step()
@@ -383,6 +384,7 @@ def measure(wl: str, args, device, world: int, steps: int, warmup: int, keep: bo
                 e1.record(stream)
                 pairs.append((e0, e1))
             torch.cuda.synchronize(device)
+            per_step.extend(a.elapsed_time(b) for a, b in pairs)
             return sum(a.elapsed_time(b) for a, b in pairs)
     else:
         for _ in range(warmup):
@@ -400,7 +402,8 @@ def measure(wl: str, args, device, world: int, steps: int, warmup: int, keep: bo
                 sort_call()
                 e1.record(stream)
                 e1.synchronize()
-                total_ms += e0.elapsed_time(e1)
+                per_step.append(e0.elapsed_time(e1))
+                total_ms += per_step[-1]
             return total_ms
 
     barrier(world, device)
@@ -410,6 +413,7 @@ def measure(wl: str, args, device, world: int, steps: int, warmup: int, keep: bo
         launches0 = om.om_launch_count()
         ms = timed_loop(steps)
         launches = om.om_launch_count() - launches0
+        call_ms = sorted(per_step)
         # ... then the same loop once more with the launch trace on, for the
         # kernels' own durations (its events sit around every launch, so the
         # call time is not taken from this loop)
@@ -455,6 +459,8 @@ def measure(wl: str, args, device, world: int, steps: int, warmup: int, keep: bo
         "achieved_gbs": (round(units_per_step * bytes_per_elem * steps / (ms / 1e3) / 1e9, 1)
                          if wl not in SORTS else None),
         "flushed": flush is not None, "roofline": roofline, "launches": launches, "clocks": clocks,
+        "ms_per_step_median": round(statistics.median(call_ms), 5) if call_ms else None,
+        "ms_per_step_min": round(call_ms[0], 5) if call_ms else None,
         "kernel_time_ms": {"tile_merge_ms": round(tm_ms, 4), "block_sort_ms": round(bs_ms, 4),
                            "block_sort_launches": bs_launches},
         "peak": peak,
@@ -486,6 +492,9 @@ def other_config_line(r: dict) -> dict:
         "clocks": {k: r["clocks"].get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "gpu_launches": r["launches"],
     }
+    if r["ms_per_step_median"] is not None:  # each call timed alone: its median and fastest call too
+        rec["ms_per_step_median"] = r["ms_per_step_median"]
+        rec["ms_per_step_min"] = r["ms_per_step_min"]
     if r["wl"] in SORTS:
         # all passes: one block pass and the late passes, each moving every pair once
         passes = 1 + r["roofline"]["launches"] // max(1, r["steps"])
@@ -687,6 +696,9 @@ def bench_ours(args):
             "gpu_launches": launches,
             "clocks": clocks,
         }
+        if r["ms_per_step_median"] is not None:  # each call timed alone (flushed merges, sorts)
+            line["ms_per_step_median"] = r["ms_per_step_median"]
+            line["ms_per_step_min"] = r["ms_per_step_min"]
         if line["achieved_gbs"] is not None:
             line["pct_of_hbm_peak"] = round(100.0 * line["achieved_gbs"] / peak, 2)
             # the same against the nominal HBM3e bandwidth of one GB300 (context)
